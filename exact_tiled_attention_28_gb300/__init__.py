@@ -1,0 +1,22 @@
+"""Exact tiled attention on one GB300 (sm_103a).
+
+Python binding of the C ABI in ``include/fa.h`` (``libfa.so``). See
+:mod:`exact_tiled_attention_28_gb300.binding`.
+"""
+
+from .binding import (  # noqa: F401
+    FA_ERR_CUDA,
+    FA_ERR_INVALID_ARG,
+    FA_ERR_TIMEOUT,
+    FA_ERR_UNSUPPORTED,
+    FA_ERR_WORKSPACE,
+    FA_OK,
+    FaError,
+    fa_bwd,
+    fa_bwd_workspace_size,
+    fa_fwd,
+    fa_last_device_status,
+    fa_status_string,
+    library_path,
+    load,
+)

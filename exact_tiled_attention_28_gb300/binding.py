@@ -1,0 +1,156 @@
+"""ctypes binding of libfa.so (the C ABI in include/fa.h).
+
+Argument marshalling only: every step of the attention computation runs in
+the library's CUDA kernels. There is no fallback of any kind; if the library
+is missing or fails to load, every call raises.
+
+The tensor-level helpers take ``torch`` CUDA tensors (PyTorch provides device
+memory and streams here, nothing else) and pass their raw device pointers,
+sizes and the current CUDA stream to the C functions of the same names.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_WORKSPACE = 5
+
+# every symbol include/fa.h declares
+EXPORTED = ("fa_abi_version", "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_status_string",
+            "fa_last_device_status")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string_safe(status)}")
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+
+def load():
+    """Loads libfa.so (once) and declares the C signatures. Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise FaError(FA_ERR_CUDA, f"{path} is not built; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_abi_version.restype = i
+    lib.fa_abi_version.argtypes = []
+    lib.fa_fwd.restype = i
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_last_device_status.restype = i
+    lib.fa_last_device_status.argtypes = [vp]
+    _lib = lib
+    return lib
+
+
+def status_string_safe(status: int) -> str:
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except Exception:  # the library itself failed to load
+        return f"status {status}"
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != FA_OK:
+        raise FaError(status, where)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    return tuple(int(x) for x in q.shape)
+
+
+def _dev_ptr(t, name, dtype, shape):
+    import torch
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous with shape {tuple(shape)}")
+    del torch
+    return t.data_ptr()
+
+
+# ---------------------------------------------------------------------------
+# raw-pointer calls (the C ABI as is)
+
+def fa_fwd_raw(q, k, v, o, lse, B, H, N, d, causal, scale, stream) -> int:
+    return load().fa_fwd(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale), stream)
+
+
+def fa_bwd_raw(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+               workspace_bytes, stream) -> int:
+    return load().fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, int(bool(causal)),
+                         float(scale), workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_last_device_status(stream=None) -> int:
+    return int(load().fa_last_device_status(_stream_handle(stream)))
+
+
+# ---------------------------------------------------------------------------
+# tensor-level calls
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """o, lse <- attention(q, k, v) on the current (or given) CUDA stream."""
+    import torch
+    B, H, N, d = _shape(q)
+    bf = torch.bfloat16
+    args = [_dev_ptr(t, n, bf, (B, H, N, d)) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
+    args.append(_dev_ptr(lse, "lse", torch.float32, (B, H, N)))
+    _check(fa_fwd_raw(*args, B, H, N, d, causal, scale, _stream_handle(stream)), "fa_fwd")
+
+
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace,
+           stream=None) -> None:
+    """dq, dk, dv <- gradients of sum(o * do); workspace is a CUDA uint8 tensor of at
+    least fa_bwd_workspace_size(B, H, N, d) bytes."""
+    import torch
+    B, H, N, d = _shape(q)
+    bf = torch.bfloat16
+    ptrs = [_dev_ptr(t, n, bf, (B, H, N, d))
+            for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
+    ptrs.append(_dev_ptr(lse, "lse", torch.float32, (B, H, N)))
+    ptrs += [_dev_ptr(t, n, bf, (B, H, N, d))
+             for t, n in ((do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))]
+    if not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    _check(fa_bwd_raw(*ptrs, B, H, N, d, causal, scale, workspace.data_ptr(),
+                      workspace.numel(), _stream_handle(stream)), "fa_bwd")

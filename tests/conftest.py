@@ -1,0 +1,24 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The built CUDA library through its Python binding (GPU tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without a CUDA device")
+    import exact_tiled_attention_28_gb300 as fa
+    fa.load()  # raises if the library is missing: no fallback
+    return fa
