@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Attention throughput on one GB300: forward + backward TFLOP/s of the CUDA
+kernels behind the C ABI, with the forward and the dK/dV kernel timed on their
+own, a roofline figure for the dominant kernel, an end-to-end figure through
+host buffers, and the fp64 CPU oracle timed on a bounded sample.
+
+One step = fa_fwd + fa_bwd (all stages) over one batch of seeded synthetic
+bf16 inputs. FLOPs: forward 4*B*H*N^2*d (halved when causal), backward 2.5x
+that, so a step counts 3.5x the forward FLOPs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--causal] [--impl reference]
+
+Under torchrun (--gpus N > 1) every rank runs an independent replica of the
+workload on its own GPU (attention heads are independent; there is no
+data-path collective) and rank 0 prints one JSON line: value = all ranks'
+FLOPs / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd+bwd (bf16, 1 GB300)"
+
+# name -> (B, H, N, d); the GPT-style sweeps keep B*N = 16384 tokens
+WORKLOADS = {"b1_h2_n128_d64": (1, 2, 128, 64), "b4_h8_n1024_d64": (4, 8, 1024, 64),
+             "long_b1_h16_n32768_d128": (1, 16, 32768, 128)}
+for _d, _H in ((64, 32), (128, 16)):
+    for _N in (512, 1024, 2048, 4096, 8192, 16384):
+        WORKLOADS[f"gpt_d{_d}_n{_N}"] = (16384 // _N, _H, _N, _d)
+DEFAULT_WORKLOAD = "gpt_d128_n4096"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dK/dV kernel,
+# from an ncu capture of the current kernel source (see profiles/), keyed by
+# workload and causal flag; None where no capture of the current kernel exists.
+NCU_TRAFFIC_BYTES: dict = {}
+
+
+def fwd_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2.0 if causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"burst": float(p["bf16_tflops"]),
+                "sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"burst": 1900.0, "sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and self.uuid not in parts[1]:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores (bounded sample)
+
+def oracle_sample(B, H, N, d, causal, seed, budget_s, max_heads):
+    """Times oracle forward + backward on whole heads of the workload until
+    budget_s has passed (at least one head). Returns (TFLOP/s, heads, seconds)."""
+    import oracle
+    from exact_tiled_attention_28_gb300 import inputs
+    scale = 1.0 / math.sqrt(d)
+    heads, spent = 0, 0.0
+    while heads < max_heads and (heads == 0 or spent < budget_s):
+        b, h = divmod(heads % (B * H), H)
+        x = inputs.head_inputs_f64(seed, b, h, N, d)
+        t0 = time.perf_counter()
+        oracle.head_forward(x["q"], x["k"], x["v"], causal, scale)
+        oracle.head_backward(x["q"], x["k"], x["v"], x["do"], causal, scale)
+        spent += time.perf_counter() - t0
+        heads += 1
+    flops = 3.5 * fwd_flops(1, 1, N, d, causal) * heads
+    return flops / spent / 1e12, heads, spent
+
+
+def cpu_cores():
+    n = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n and n.isdigit() else os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def config_of(args, B, H, N, d):
+    return {"workload": f"{args.workload}: B={B} H={H} N={N} d={d} "
+                        f"{'causal' if args.causal else 'non-causal'} fwd+bwd",
+            "B": B, "H": H, "N": N, "d": d, "causal": bool(args.causal),
+            "scale": "1/sqrt(d)", "global_batch": B * args.gpus, "seq_len": N,
+            "parallelism": f"replicas x{args.gpus}",
+            "l2": "inputs larger than L2" if 8 * B * H * N * d * 2 > 129e6 else "L2-resident"}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle as it stands, on the host cores."""
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    B, H, N, d = WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        oracle_sample(B, H, N, d, args.causal, 1000, 0.0, 1)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        oracle_sample(B, H, N, d, args.causal, 1000, 0.0, 1)
+        flops += 3.5 * fwd_flops(1, 1, N, d, args.causal)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(args, B, H, N, d),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                             "kind": "oracle",
+                             "sample": f"one head (N={N}, d={d}) fwd+bwd per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    import exact_tiled_attention_28_gb300 as fa
+    from exact_tiled_attention_28_gb300 import inputs
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    fa.load()  # raises if the library is missing: there is no fallback
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, H, N, d = WORKLOADS[args.workload]
+    causal = bool(args.causal)
+    scale = 1.0 / math.sqrt(d)
+    seed = 1000 + rank
+
+    bits = inputs.attention_inputs(seed, B, H, N, d)
+    host = {n: inputs.bits_to_torch_bf16(b).pin_memory() for n, b in bits.items()}
+    x = {n: t.to(dev) for n, t in host.items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, causal, scale)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_stages(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, causal, scale, ws,
+                         events=None if ev is None else ev[2:6])
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status reports a timeout during warm-up")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status reports a timeout in the timed region")
+    ms_total = t_start.elapsed_time(t_end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    pre_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    dkdv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+    dq_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[5]) for e in evs)
+    ms_step = ms_total / args.steps
+
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step_max = float(t.item())
+    else:
+        ms_step_max = ms_step
+
+    # end to end through host buffers: pinned inputs in, every output back
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for n in host:
+            x[n].copy_(host[n], non_blocking=True)
+        fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, causal, scale)
+        fa.fa_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, causal, scale, ws)
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_host[n].copy_(t, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+
+    F = fwd_flops(B, H, N, d, causal)
+    peaks = load_peaks()
+    tag = "of " + peaks["source"]
+    value = world * 3.5 * F / (ms_step_max * 1e-3) / 1e12
+    dkdv_tf = 2.5 * F / (dkdv_ms * 1e-3) / 1e12
+    fwd_tf = F / (fwd_ms * 1e-3) / 1e12
+    traffic = NCU_TRAFFIC_BYTES.get((args.workload, causal))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: Q, K, V, dO i.i.d. N(0,1) rounded to bf16, seeded",
+        "config": config_of(args, B, H, N, d),
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf,
+                "frac_of_burst_peak": fwd_tf / peaks["burst"],
+                "frac_of_sustained_peak": fwd_tf / peaks["sustained"]},
+        "fwd_bwd": {"tflops": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+                    "frac_of_burst_peak": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peaks["burst"],
+                    "frac_of_sustained_peak": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peaks["sustained"]},
+        "bwd": {"ms": bwd_ms, "pre_ms": pre_ms, "dkdv_ms": dkdv_ms, "dq_ms": dq_ms,
+                "tflops": 2.5 * F / (bwd_ms * 1e-3) / 1e12},
+        "roofline": {"kernel": "bwd_dkdv_kernel", "bound": "tensor", "achieved": dkdv_tf,
+                     "peak": peaks["sustained"], "unit": "TFLOP/s",
+                     "frac": dkdv_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}",
+                     "traffic": traffic,
+                     "algorithmic": f"2.5 x 4*B*H*N^2*d{' / 2' if causal else ''} = {2.5 * F:.4g} FLOP per launch"},
+        "roofline_fwd": {"kernel": "fwd_kernel", "bound": "tensor", "achieved": fwd_tf,
+                         "peak": peaks["sustained"], "unit": "TFLOP/s",
+                         "frac": fwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}"},
+        "e2e": {"value": 3.5 * F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if world > 1:
+        torch.distributed.barrier()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, heads, spent = oracle_sample(B, H, N, d, causal, seed, args.cpu_budget_s, 64)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"{heads} whole heads (N={N}, d={d}) fwd+bwd, "
+                                          f"{spent:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

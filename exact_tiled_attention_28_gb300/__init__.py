@@ -13,9 +13,11 @@ from .binding import (  # noqa: F401
     FA_OK,
     FaError,
     fa_bwd,
+    fa_bwd_stages,
     fa_bwd_workspace_size,
     fa_fwd,
     fa_last_device_status,
+    fa_selftest_wait_timeout,
     fa_status_string,
     library_path,
     load,

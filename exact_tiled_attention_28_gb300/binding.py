@@ -22,7 +22,8 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
 
 # every symbol include/fa.h declares
-EXPORTED = ("fa_abi_version", "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_status_string",
+EXPORTED = ("fa_abi_version", "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess",
+            "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_selftest_wait_timeout", "fa_status_string",
             "fa_last_device_status")
 
 _lib = None
@@ -56,6 +57,14 @@ def load():
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_preprocess.restype = i
+    lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
+    lib.fa_bwd_dkdv.restype = i
+    lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_dq_finalize.restype = i
+    lib.fa_bwd_dq_finalize.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_selftest_wait_timeout.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [i]
     lib.fa_last_device_status.restype = i
@@ -117,8 +126,28 @@ def fa_bwd_raw(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, causal, scale, works
                          float(scale), workspace, workspace_bytes, stream)
 
 
+def fa_bwd_preprocess_raw(o, lse, do, B, H, N, d, workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd_preprocess(o, lse, do, B, H, N, d, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_dkdv_raw(q, k, v, do, dk, dv, B, H, N, d, causal, scale, workspace, workspace_bytes,
+                    stream) -> int:
+    return load().fa_bwd_dkdv(q, k, v, do, dk, dv, B, H, N, d, int(bool(causal)), float(scale),
+                              workspace, workspace_bytes, stream)
+
+
+def fa_bwd_dq_finalize_raw(dq, B, H, N, d, scale, workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd_dq_finalize(dq, B, H, N, d, float(scale), workspace, workspace_bytes,
+                                     stream)
+
+
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
+    _check(load().fa_selftest_wait_timeout(int(limit_ms), _stream_handle(stream)),
+           "fa_selftest_wait_timeout")
 
 
 def fa_last_device_status(stream=None) -> int:
@@ -154,3 +183,32 @@ def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspac
         raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
     _check(fa_bwd_raw(*ptrs, B, H, N, d, causal, scale, workspace.data_ptr(),
                       workspace.numel(), _stream_handle(stream)), "fa_bwd")
+
+
+def fa_bwd_stages(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace,
+                  stream=None, events=None) -> None:
+    """fa_bwd as its three C-ABI stages. If ``events`` is a list of four CUDA
+    events, they are recorded before, between and after the stages (the
+    benchmark times the dK/dV stage with them)."""
+    import torch
+    B, H, N, d = _shape(q)
+    bf = torch.bfloat16
+    shp = (B, H, N, d)
+    P = {n: _dev_ptr(t, n, bf, shp) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"),
+                                                  (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))}
+    pl = _dev_ptr(lse, "lse", torch.float32, (B, H, N))
+    ws, nws = workspace.data_ptr(), workspace.numel()
+    st = _stream_handle(stream)
+    s = torch.cuda.current_stream() if stream is None else stream
+    if events:
+        events[0].record(s)
+    _check(fa_bwd_preprocess_raw(P["o"], pl, P["do"], B, H, N, d, ws, nws, st), "fa_bwd_preprocess")
+    if events:
+        events[1].record(s)
+    _check(fa_bwd_dkdv_raw(P["q"], P["k"], P["v"], P["do"], P["dk"], P["dv"], B, H, N, d, causal,
+                           scale, ws, nws, st), "fa_bwd_dkdv")
+    if events:
+        events[2].record(s)
+    _check(fa_bwd_dq_finalize_raw(P["dq"], B, H, N, d, scale, ws, nws, st), "fa_bwd_dq_finalize")
+    if events:
+        events[3].record(s)

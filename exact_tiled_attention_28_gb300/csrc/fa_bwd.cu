@@ -1,0 +1,617 @@
+// Backward kernels: recompute S and P per tile, then dP, dS, dV, dK, dQ.
+//
+// What it computes ("Flash Attention v2" notes, "Backward Pass Computation":
+// recompute S block by block from Q and K, then the gradients block by
+// block, never materialising N x N matrices; the softmax Jacobian is the full
+// one, not the diagonal form printed there):
+//   D_i = sum_c dO_ic O_ic                       (pre-pass)
+//   P_ij = exp(scale q_i.k_j - lse_i)            (recomputed from the forward's lse)
+//   dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i)
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K
+//
+// GB300 mapping:
+//  1. bwd_pre_kernel (memory bound): D, the log-sum-exp in log2 units, both
+//     padded to whole 128-row tiles (pad rows: D = 0, lse2 = +inf so that P
+//     vanishes there), and zeroes the fp32 dQ accumulator.
+//  2. bwd_dkdv_kernel: persistent CTAs over (batch*head, key block j). A CTA
+//     keeps K_j and V_j in shared memory and dV_j, dK_j in tensor memory and
+//     loops over the query blocks i (causal: i >= j, longest blocks first):
+//       S^T = K_j Q_i^T and dP^T = V_j dO_i^T       (tcgen05, SS)
+//       P^T, dS^T by the compute warps, one thread per key row  (TMEM <-> regs)
+//       dV += P^T dO_i and dK += dS^T Q_i           (tcgen05, A from TMEM)
+//       dQ_i = dS K_j                               (tcgen05, A = dS^T in SMEM)
+//     and four more warps read dQ_i out of TMEM and add it to the fp32
+//     accumulator in global memory (vector atomics).
+//  3. dq_convert_kernel: dq = bf16(scale * accumulator).
+//
+// TMEM (512 columns): S^T/P^T [0,128), dP^T/dS^T then dQ_i [128,256),
+// dV [256, 256+d), dK [256+d, 256+2d).
+
+#include <algorithm>
+
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 320;  // 4 compute warps, 4 dQ warps, load warp, MMA warp
+constexpr int kBwdLoadWarp = 8;
+constexpr int kBwdMmaWarp = 9;
+constexpr uint32_t kBwdTmemCols = 512;
+constexpr int kBlk = kTile * 64 * 2;  // 16 KiB: one 128-row x 64-column bf16 block
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;
+constexpr int kSmemSpare = 768;  // bytes left for aligning the dynamic base to 1024
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kColBlocks = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kStageBytes = 2 * kTileBytes + 1024;  // Q_i, dO_i, lse2 and D rows
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffDS = 2 * kTileBytes;             // dS^T, 128 x 128 bf16
+  static constexpr int kOffStages = 2 * kTileBytes + kTile * kTile * 2;
+  static constexpr int kOffBars = kOffStages + kStages * kStageBytes;
+  static constexpr uint32_t col_dk() { return kColDV + D; }
+};
+
+struct BwdBarriers {
+  uint64_t kv_full, kv_empty;
+  uint64_t st_full[2], st_empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+constexpr int bwd_smem_bytes() {
+  return BwdCfg<D>::kOffBars + static_cast<int>(sizeof(BwdBarriers)) + kSmemSpare;
+}
+static_assert(bwd_smem_bytes<128>() <= 232448, "backward shared memory over the sm_103a limit");
+static_assert(bwd_smem_bytes<64>() <= 232448, "backward shared memory over the sm_103a limit");
+
+struct BwdArgs {
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dO;
+  const float* lse;
+  float* Drow;    // [BH, Npad]
+  float* lse2;    // [BH, Npad]
+  float* dq_acc;  // [BH, N, d]
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  int N, Npad, BH, n_tiles, n_items;
+  float scale, scale_log2;
+};
+
+// ---------------------------------------------------------------------------
+// 1. pre-pass
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  constexpr int kLanesPerRow = D / 8;  // each lane handles 8 elements (16 bytes)
+  const size_t rows = static_cast<size_t>(a.BH) * a.Npad;
+  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       g < rows * kLanesPerRow; g += nthreads) {
+    const size_t row = g / kLanesPerRow;
+    const int part = static_cast<int>(g % kLanesPerRow);
+    const int bh = static_cast<int>(row / a.Npad);
+    const int i = static_cast<int>(row % a.Npad);
+    float dot = 0.f;
+    if (i < a.N) {
+      const size_t e = (static_cast<size_t>(bh) * a.N + i) * D + part * 8;
+      const uint4 ov = *reinterpret_cast<const uint4*>(a.o + e);
+      const uint4 gv = *reinterpret_cast<const uint4*>(a.dO + e);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 of = __bfloat1622float2(o2[u]);
+        const float2 gf = __bfloat1622float2(g2[u]);
+        dot = fmaf(of.x, gf.x, dot);
+        dot = fmaf(of.y, gf.y, dot);
+      }
+      float4* z = reinterpret_cast<float4*>(a.dq_acc + e);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // reduce over the kLanesPerRow consecutive lanes of this row
+#pragma unroll
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+      dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (part == 0) {
+      a.Drow[row] = dot;
+      a.lse2[row] = (i < a.N) ? a.lse[static_cast<size_t>(bh) * a.N + i] * 1.4426950408889634f
+                              : __int_as_float(0x7f800000);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. dq = bf16(scale * accumulator)
+
+__global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a, size_t n8) {
+  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n8;
+       g += nthreads) {
+    const float4* src = reinterpret_cast<const float4*>(a.dq_acc) + 2 * g;
+    const float4 x = src[0], y = src[1];
+    uint4 w;
+    w.x = pack_bf16x2(x.x * a.scale, x.y * a.scale);
+    w.y = pack_bf16x2(x.z * a.scale, x.w * a.scale);
+    w.z = pack_bf16x2(y.x * a.scale, y.y * a.scale);
+    w.w = pack_bf16x2(y.z * a.scale, y.w * a.scale);
+    reinterpret_cast<uint4*>(a.dq)[g] = w;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. dK / dV (and dQ contributions)
+
+__device__ __forceinline__ void decode_kv_item(int item, const BwdArgs& a, bool causal, int& bh,
+                                               int& j) {
+  if (causal) {  // key block 0 visits every query block: longest first
+    j = item / a.BH;
+    bh = item % a.BH;
+  } else {  // blocks of one head adjacent: Q and dO shared through L2
+    bh = item / a.n_tiles;
+    j = item % a.n_tiles;
+  }
+}
+
+__device__ __forceinline__ void cp_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                    const BwdArgs a) {
+  using Cfg = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  const uintptr_t aligned = (raw + 1023) & ~static_cast<uintptr_t>(1023);
+  if (aligned - raw > kSmemSpare) {  // cannot happen with a 1 KiB-aligned dynamic base
+    if (threadIdx.x == 0) atomicCAS(a.status, DEV_OK, DEV_TIMEOUT);
+    return;
+  }
+  uint8_t* smem = reinterpret_cast<uint8_t*>(aligned);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase + Cfg::kOffK, sV = sbase + Cfg::kOffV, sDS = sbase + Cfg::kOffDS;
+  const uint32_t sSt = sbase + Cfg::kOffStages;
+  BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(smem + Cfg::kOffBars);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_q = a.n_tiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->kv_full), 1);
+    mbar_init(smem_u32(&bars->kv_empty), 1);
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(smem_u32(&bars->st_full[s]), 1);
+      mbar_init(smem_u32(&bars->st_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->dp_full), 1);
+    mbar_init(smem_u32(&bars->p_ready), 128);
+    mbar_init(smem_u32(&bars->ds_ready), 128);
+    mbar_init(smem_u32(&bars->dq_full), 1);
+    mbar_init(smem_u32(&bars->dq_free), 128);
+    mbar_init(smem_u32(&bars->acc_done), 1);
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kBwdLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kBwdLoadWarp) {
+    // ---------------------------------------------------------------- loader
+    if (lane == 0) {
+      const uint64_t pol_kv = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      uint32_t st_it = 0, kv_round = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+        int bh, j;
+        decode_kv_item(item, a, CAUSAL, bh, j);
+        ok = mbar_wait(smem_u32(&bars->kv_empty), (kv_round & 1) ^ 1, abort, a.status);
+        if (!ok) break;
+        {
+          const uint32_t bar = smem_u32(&bars->kv_full);
+          mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
+          for (int cb = 0; cb < Cfg::kColBlocks; ++cb) {
+            tma_load_3d(sK + cb * kBlk, &tmK, bar, 64 * cb, j * kTile, bh, pol_kv);
+            tma_load_3d(sV + cb * kBlk, &tmV, bar, 64 * cb, j * kTile, bh, pol_kv);
+          }
+          ++kv_round;
+        }
+        for (int i = CAUSAL ? j : 0; i < n_q && ok; ++i) {
+          const uint32_t s = st_it % Cfg::kStages;
+          ok = mbar_wait(smem_u32(&bars->st_empty[s]), ((st_it / Cfg::kStages) & 1) ^ 1, abort,
+                         a.status);
+          if (!ok) break;
+          const uint32_t bar = smem_u32(&bars->st_full[s]);
+          const uint32_t st = sSt + s * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes + 1024);
+          for (int cb = 0; cb < Cfg::kColBlocks; ++cb) {
+            tma_load_3d(st + cb * kBlk, &tmQ, bar, 64 * cb, i * kTile, bh, pol_q);
+            tma_load_3d(st + Cfg::kTileBytes + cb * kBlk, &tmdO, bar, 64 * cb, i * kTile, bh,
+                        pol_q);
+          }
+          const size_t roff = static_cast<size_t>(bh) * a.Npad + static_cast<size_t>(i) * kTile;
+          cp_bulk_g2s(st + 2 * Cfg::kTileBytes, a.lse2 + roff, 512, bar);
+          cp_bulk_g2s(st + 2 * Cfg::kTileBytes + 512, a.Drow + roff, 512, bar);
+          ++st_it;
+        }
+      }
+      // producer tail (see the forward kernel)
+      const uint32_t n = min(st_it, static_cast<uint32_t>(Cfg::kStages));
+      for (uint32_t u = st_it - n; u < st_it; ++u) {
+        const uint32_t s = u % Cfg::kStages, ph = (u / Cfg::kStages) & 1;
+        if (ok) ok = mbar_wait(smem_u32(&bars->st_empty[s]), ph, abort, a.status);
+        if (!ok) mbar_drain(smem_u32(&bars->st_full[s]), ph, 100000000ull);
+      }
+      if (kv_round > 0) {
+        const uint32_t ph = (kv_round - 1) & 1;
+        if (ok) ok = mbar_wait(smem_u32(&bars->kv_empty), ph, abort, a.status);
+        if (!ok) mbar_drain(smem_u32(&bars->kv_full), ph, 100000000ull);
+      }
+    }
+  } else if (warp == kBwdMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      // S^T = K Q^T, dP^T = V dO^T: M = 128 keys, N = 128 queries, K-major operands
+      constexpr uint32_t idesc_kq = idesc_bf16_f32(kTile, kTile, false, false);
+      // dV += P^T dO, dK += dS^T Q: A from TMEM, B MN-major, N = d
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(kTile, D, false, true);
+      // dQ = dS K: A = dS^T in SMEM (MN-major), B = K MN-major, N = d
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(kTile, D, true, true);
+      uint32_t st_it = 0, kv_round = 0, it = 0;
+      bool ok = true;
+
+      auto issue_kq = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
+          mma_ss(dst, smem_desc_sw128(a_tile + off, 16, 1024),
+                 smem_desc_sw128(b_tile + off, 16, 1024), idesc_kq, kk > 0);
+        }
+      };
+      auto issue_acc = [&](uint32_t dst, uint32_t a_tmem, uint32_t b_tile, bool accumulate) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(dst, a_tmem + kk * 8, smem_desc_sw128(b_tile + kk * 2048, kBlk, 1024), idesc_acc,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
+      auto issue_dq = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(tmem + kColDP, smem_desc_sw128(sDS + kk * 2048, kBlk, 1024),
+                 smem_desc_sw128(sK + kk * 2048, kBlk, 1024), idesc_dq, kk > 0);
+      };
+
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++kv_round) {
+        int bh, j;
+        decode_kv_item(item, a, CAUSAL, bh, j);
+        const int i0 = CAUSAL ? j : 0;
+        const int n_it = n_q - i0;
+        ok = mbar_wait(smem_u32(&bars->kv_full), kv_round & 1, abort, a.status);
+        if (!ok) break;
+        // prologue: S^T(0), dP^T(0); dP needs the dQ readout of the previous item done
+        uint32_t s0 = st_it % Cfg::kStages;
+        ok = mbar_wait(smem_u32(&bars->st_full[s0]), (st_it / Cfg::kStages) & 1, abort, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t stq = sSt + s0 * Cfg::kStageBytes;
+        issue_kq(tmem + kColS, sK, stq);
+        mma_commit(smem_u32(&bars->s_full));
+        if (it > 0) {
+          ok = mbar_wait(smem_u32(&bars->dq_free), (it - 1) & 1, abort, a.status);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_kq(tmem + kColDP, sV, stq + Cfg::kTileBytes);
+        mma_commit(smem_u32(&bars->dp_full));
+        for (int u = 0; u < n_it && ok; ++u, ++it, ++st_it) {
+          const uint32_t s = st_it % Cfg::kStages;
+          const uint32_t stage = sSt + s * Cfg::kStageBytes;
+          const bool has_next = u + 1 < n_it;
+          const uint32_t sn = (st_it + 1) % Cfg::kStages;
+          const uint32_t next = sSt + sn * Cfg::kStageBytes;
+          ok = mbar_wait(smem_u32(&bars->p_ready), it & 1, abort, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_acc(tmem + kColDV, tmem + kColS, stage + Cfg::kTileBytes, u > 0);  // dV += P^T dO
+          if (has_next) {
+            ok = mbar_wait(smem_u32(&bars->st_full[sn]), ((st_it + 1) / Cfg::kStages) & 1, abort,
+                           a.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_kq(tmem + kColS, sK, next);  // S^T(u+1)
+            mma_commit(smem_u32(&bars->s_full));
+          }
+          ok = mbar_wait(smem_u32(&bars->ds_ready), it & 1, abort, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_acc(tmem + Cfg::col_dk(), tmem + kColDP, stage, u > 0);  // dK += dS^T Q
+          issue_dq();                                                    // dQ_i = dS K
+          mma_commit(smem_u32(&bars->dq_full));
+          mma_commit(smem_u32(&bars->st_empty[s]));
+          if (!has_next) {
+            mma_commit(smem_u32(&bars->acc_done));
+            mma_commit(smem_u32(&bars->kv_empty));
+          } else {
+            ok = mbar_wait(smem_u32(&bars->dq_free), it & 1, abort, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_kq(tmem + kColDP, sV, next + Cfg::kTileBytes);  // dP^T(u+1)
+            mma_commit(smem_u32(&bars->dp_full));
+          }
+        }
+      }
+      mma_commit(smem_u32(&bars->drain));
+      mbar_drain(smem_u32(&bars->drain), 0, 1000000000ull);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------ compute warps: P^T and dS^T
+    const int r = warp * 32 + lane;  // key row within the block = TMEM lane
+    const uint32_t t_lane = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
+    const float sl2 = a.scale_log2;
+    uint32_t st_it = 0, it = 0, kv_round = 0;
+    bool ok = true;
+    // swizzled row of dS^T in shared memory: 128-byte rows, 16-byte chunks XOR (row & 7)
+    const uint32_t ds_row = sDS + r * 128;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++kv_round) {
+      int bh, j;
+      decode_kv_item(item, a, CAUSAL, bh, j);
+      const int i0 = CAUSAL ? j : 0;
+      const int n_it = n_q - i0;
+      for (int u = 0; u < n_it; ++u, ++it, ++st_it) {
+        const int i = i0 + u;
+        const uint32_t s = st_it % Cfg::kStages;
+        const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kOffStages +
+                                                           s * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
+        const float* Dq = lse2 + 128;
+        // phase A: P^T = exp2(S^T * scale*log2e - lse2[q]), causal mask on the diagonal
+        ok = mbar_wait_warp(smem_u32(&bars->s_full), it & 1, abort, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld128(t_lane + kColS, sr);
+        const bool diag = CAUSAL && i == j;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 2 * c);
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -l2.x));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -l2.y));
+          if (diag) {  // query q sees key r only if r <= q
+            p0 = (2 * c < r) ? 0.f : p0;
+            p1 = (2 * c + 1 < r) ? 0.f : p1;
+          }
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st64(t_lane + kColS, pk);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->p_ready));
+        // phase B: dS^T = P^T o (dP^T - D[q]); needs the previous dQ MMA done
+        // with the dS buffer (its completion precedes dP^T(i) in MMA order)
+        ok = mbar_wait_warp(smem_u32(&bars->dp_full), it & 1, abort, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        // 32 queries at a time: dP^T chunk in, dS^T chunk out to TMEM and SMEM
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t dp[32];
+          tmem_ld32(t_lane + kColDP + 32 * h, dp);
+          uint32_t ds[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int q = 32 * h + 2 * c;
+            const float2 pf =
+                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[16 * h + c]));
+            const float2 dd = *reinterpret_cast<const float2*>(Dq + q);
+            ds[c] = pack_bf16x2(pf.x * (__uint_as_float(dp[2 * c]) - dd.x),
+                                pf.y * (__uint_as_float(dp[2 * c + 1]) - dd.y));
+          }
+          tmem_st16(t_lane + kColDP + 16 * h, ds);
+          // dS^T row r, queries 32h..32h+31: query block cb = h / 2, 16-byte
+          // chunks ch = 4 (h % 2) .. +3, stored at chunk ch ^ (r & 7)
+#pragma unroll
+          for (int u4 = 0; u4 < 4; ++u4) {
+            const int ch = 4 * (h & 1) + u4;
+            const uint32_t addr = ds_row + (h >> 1) * kBlk + ((ch ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(ds[4 * u4]),
+                         "r"(ds[4 * u4 + 1]), "r"(ds[4 * u4 + 2]), "r"(ds[4 * u4 + 3])
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->ds_ready));
+      }
+      if (!ok) break;
+      // epilogue: dV and scale * dK of this key block
+      ok = mbar_wait_warp(smem_u32(&bars->acc_done), kv_round & 1, abort, a.status);
+      if (!ok) break;
+      tc_fence_after();
+      const int key = j * kTile + r;
+      const bool store = key < a.N;
+      const size_t base = (static_cast<size_t>(bh) * a.N + key) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* out = (which == 0 ? a.dv : a.dk) + base;
+        const float mul = which == 0 ? 1.f : a.scale;
+        const uint32_t col = which == 0 ? kColDV : Cfg::col_dk();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(t_lane + col + cc * 32, v);
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(out + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+              w.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+              w.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+              w.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+              dst[v4] = w;
+            }
+          }
+        }
+      }
+      // the next item's first dV/dK MMAs overwrite these accumulators only
+      // after p_ready/ds_ready of that item, which this warpgroup signals later
+    }
+  } else {
+    // ------------------------------------------------- dQ warps: add dQ_i
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query row within the block
+    const uint32_t t_lane = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      int bh, j;
+      decode_kv_item(item, a, CAUSAL, bh, j);
+      const int i0 = CAUSAL ? j : 0;
+      for (int i = i0; i < n_q; ++i, ++it) {
+        ok = mbar_wait_warp(smem_u32(&bars->dq_full), it & 1, abort, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[D];
+        if constexpr (D == 128) {
+          tmem_ld128(t_lane + kColDP, v);
+        } else {
+          uint32_t t32[32];
+          tmem_ld32(t_lane + kColDP, t32);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = t32[c];
+          tmem_ld32(t_lane + kColDP + 32, t32);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[32 + c] = t32[c];
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->dq_free));
+        const int row = i * kTile + r;
+        if (row < a.N) {
+          float4* dst = reinterpret_cast<float4*>(a.dq_acc + (static_cast<size_t>(bh) * a.N + row) * D);
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c)
+            atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                           __uint_as_float(v[4 * c + 2]),
+                                           __uint_as_float(v[4 * c + 3])));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kBwdMmaWarp) tmem_dealloc(tmem, kBwdTmemCols);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const BwdArgs& a,
+                         int stages, cudaStream_t stream) {
+  if (stages & kStagePre) {
+    const size_t work = static_cast<size_t>(a.BH) * a.Npad * (D / 8);
+    const int grid = static_cast<int>(std::min<size_t>((work + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
+    bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kStageDkdv) {
+    constexpr int smem = bwd_smem_bytes<D>();
+    auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = min(a.n_items, p.num_sms);
+    kern<<<grid, kBwdThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kStageDq) {
+    const size_t n8 = static_cast<size_t>(a.BH) * a.N * D / 8;
+    const int grid = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
+    dq_convert_kernel<<<grid, 256, 0, stream>>>(a, n8);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int H, int N, int d) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t Npad = (static_cast<size_t>(N) + kTile - 1) / kTile * kTile;
+  return 2 * BH * Npad * 4 + BH * static_cast<size_t>(N) * d * 4;
+}
+
+cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const void* v,
+                       const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                       void* dv, void* workspace, int stages, cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  CUtensorMap maps[4];
+  if ((stages & kStageDkdv) &&
+      (!make_tile_map(&maps[0], q, BH, p.N, p.d) || !make_tile_map(&maps[1], k, BH, p.N, p.d) ||
+       !make_tile_map(&maps[2], v, BH, p.N, p.d) || !make_tile_map(&maps[3], dO, BH, p.N, p.d)))
+    return cudaErrorInvalidValue;
+  BwdArgs a;
+  a.n_tiles = (p.N + kTile - 1) / kTile;
+  a.Npad = a.n_tiles * kTile;
+  a.N = p.N;
+  a.BH = BH;
+  a.n_items = BH * a.n_tiles;
+  a.o = static_cast<const __nv_bfloat16*>(o);
+  a.dO = static_cast<const __nv_bfloat16*>(dO);
+  a.lse = lse;
+  float* ws = static_cast<float*>(workspace);
+  a.Drow = ws;
+  a.lse2 = ws + static_cast<size_t>(BH) * a.Npad;
+  a.dq_acc = ws + 2 * static_cast<size_t>(BH) * a.Npad;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.status = p.status;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  if (p.d == 64)
+    return p.causal ? launch_bwd_t<64, true>(p, maps, a, stages, stream)
+                    : launch_bwd_t<64, false>(p, maps, a, stages, stream);
+  return p.causal ? launch_bwd_t<128, true>(p, maps, a, stages, stream)
+                  : launch_bwd_t<128, false>(p, maps, a, stages, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,466 @@
+// Forward kernel: exact attention, tile by tile, with an online softmax.
+//
+// What it computes ("flashattention-2" glossary, "How FlashAttention-2 Works
+// (Tiled Algorithm)"; "Flash Attention v2" notes, "Detailed Algorithm
+// Comparison", forward pass): for each 128-row query tile Q_i, stream the
+// 128-key tiles K_j, V_j; S = Q_i K_j^T; keep a running row max m and row sum
+// l; P = exp(scale*S - scale*m); O = alpha*O + P V_j with alpha =
+// exp(scale*(m_old - m_new)); at the end O / l and lse = scale*m + ln l.
+//
+// GB300 mapping (not the pages' A100 scheme):
+//  - persistent CTAs, one per SM, each taking work items (batch*head, pair
+//    of query tiles) in a static stride; causal items longest first
+//    ("FlashAttention-2 paper" digest, "Three changes": query blocks of one
+//    head are split across thread blocks; glossary improvements table,
+//    "Causal Masking": fully masked tiles skipped);
+//  - warp 8 issues TMA loads of Q (once per item) and of K/V tiles into a
+//    ring of shared-memory stages guarded by full/empty mbarriers;
+//  - warp 9 issues tcgen05.mma: S_t = Q_t K_j^T into tensor memory (TMEM),
+//    then O_t += P_t V_j with P_t read from TMEM (P overwrites S in place);
+//  - warps 0-3 and 4-7 are two softmax warpgroups, one per query tile, one
+//    thread per query row (the TMEM lane of that row). While one warpgroup
+//    runs its softmax the tensor core works on the other tile's products;
+//  - the rescale of O is deferred: it is applied only when the row maximum
+//    grows by more than kRescaleTauLog2 (in log2 units; 0 = every growth).
+//    O and l are always scaled by the same factor, so the result is exact in
+//    real arithmetic ("FlashAttention-2 paper" digest, "Three changes": the
+//    rescaling is delayed and batched). 1/l is applied once in the epilogue.
+//
+// TMEM (512 columns x 128 lanes of 32 bit): S0 [0,128), S1 [128,256),
+// O0 [256, 256+d), O1 [256+d, 256+2d). P_t is bf16, two per column, in the
+// first 64 columns of S_t.
+
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+#ifndef FA_RESCALE_TAU_LOG2
+#define FA_RESCALE_TAU_LOG2 8.0f
+#endif
+constexpr float kRescaleTauLog2 = FA_RESCALE_TAU_LOG2;
+
+constexpr int kFwdThreads = 320;  // 8 softmax warps + load warp + MMA warp
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBlockBytes = kTile * 64 * 2;  // one 128-row x 64-column bf16 block: 16 KiB
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kColBlocks = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kQBytes = 2 * kTileBytes;
+  static constexpr int kRingBytes = kStages * kTileBytes;
+  // TMEM column of S_t and of O_t
+  __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+  __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+};
+
+struct FwdBarriers {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[8], kv_empty[8];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+constexpr int fwd_smem_bytes() {
+  return 1024 + FwdCfg<D>::kQBytes + FwdCfg<D>::kRingBytes + static_cast<int>(sizeof(FwdBarriers));
+}
+
+struct FwdArgs {
+  __nv_bfloat16* o;
+  float* lse;
+  int* status;
+  int N, BH, n_tiles, n_pairs, n_items;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ void decode_item(int item, const FwdArgs& a, bool causal, int& bh,
+                                            int& pair) {
+  if (causal) {  // longest first: the last query pairs of every head come first
+    pair = a.n_pairs - 1 - item / a.BH;
+    bh = item % a.BH;
+  } else {  // the pairs of one head are adjacent, so concurrent CTAs share K/V in L2
+    bh = item / a.n_pairs;
+    pair = item % a.n_pairs;
+  }
+}
+
+// Number of K/V tiles query tile qt visits (0 if the tile lies past N).
+__device__ __forceinline__ int tile_steps(int qt, const FwdArgs& a, bool causal) {
+  if (qt >= a.n_tiles) return 0;
+  return causal ? min(qt + 1, a.n_tiles) : a.n_tiles;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using Cfg = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sKV = sQ + Cfg::kQBytes;
+  FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(smem + Cfg::kQBytes + Cfg::kRingBytes);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bars->q_full[t]), 1);
+      mbar_init(smem_u32(&bars->q_empty[t]), 1);
+      mbar_init(smem_u32(&bars->s_full[t]), 1);
+      mbar_init(smem_u32(&bars->p_full[t]), 128);
+      mbar_init(smem_u32(&bars->o_done[t]), 1);
+    }
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kLoadWarp) {
+    // ---------------------------------------------------------------- loader
+    if (lane == 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      uint32_t kv_it = 0;
+      uint32_t q_issued[2] = {0u, 0u};
+      bool ok = true;
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+        int bh, pair;
+        decode_item(item, a, CAUSAL, bh, pair);
+        const int J = max(tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL));
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = mbar_wait(smem_u32(&bars->q_empty[t]), (q_issued[t] & 1) ^ 1, abort, a.status);
+          if (!ok) break;
+          const uint32_t bar = smem_u32(&bars->q_full[t]);
+          mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
+          for (int cb = 0; cb < Cfg::kColBlocks; ++cb)
+            tma_load_3d(sQ + (t * Cfg::kColBlocks + cb) * kBlockBytes, &tmQ, bar, 64 * cb,
+                        (2 * pair + t) * kTile, bh, pol_q);
+          ++q_issued[t];
+        }
+        for (int j = 0; j < J && ok; ++j) {
+          for (int w = 0; w < 2; ++w) {  // K_j then V_j
+            const uint32_t s = kv_it % Cfg::kStages;
+            ok = mbar_wait(smem_u32(&bars->kv_empty[s]), ((kv_it / Cfg::kStages) & 1) ^ 1, abort,
+                           a.status);
+            if (!ok) break;
+            const uint32_t bar = smem_u32(&bars->kv_full[s]);
+            mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
+            for (int cb = 0; cb < Cfg::kColBlocks; ++cb)
+              tma_load_3d(sKV + (s * Cfg::kColBlocks + cb) * kBlockBytes, w ? &tmV : &tmK, bar,
+                          64 * cb, j * kTile, bh, pol_kv);
+            ++kv_it;
+          }
+        }
+      }
+      // Producer tail. Normal path: wait until the consumer has released every
+      // stage, so that no barrier arrival lands after the CTA exits. After an
+      // abort: wait (bounded) for the copies already issued to land.
+      const uint32_t n = min(kv_it, static_cast<uint32_t>(Cfg::kStages));
+      for (uint32_t i = kv_it - n; i < kv_it; ++i) {
+        const uint32_t s = i % Cfg::kStages, ph = (i / Cfg::kStages) & 1;
+        if (ok) ok = mbar_wait(smem_u32(&bars->kv_empty[s]), ph, abort, a.status);
+        if (!ok) mbar_drain(smem_u32(&bars->kv_full[s]), ph, 100000000ull);
+      }
+      for (int t = 0; t < 2; ++t) {
+        if (q_issued[t] == 0) continue;
+        const uint32_t ph = (q_issued[t] - 1) & 1;
+        if (ok) ok = mbar_wait(smem_u32(&bars->q_empty[t]), ph, abort, a.status);
+        if (!ok) mbar_drain(smem_u32(&bars->q_full[t]), ph, 100000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, false, true);
+      uint32_t kv_it = 0, q_round = 0;
+      uint32_t step[2] = {0u, 0u};
+      bool ok = true;
+
+      // S_t = Q_t K^T over d in steps of 16
+      auto issue_s = [&](int t, uint32_t slot) {
+        const uint32_t dst = tmem + Cfg::col_s(t);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(sQ + t * Cfg::kTileBytes + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sKV + slot * Cfg::kTileBytes + off, 16, 1024);
+          mma_ss(dst, ad, bd, idesc_s, kk > 0);
+        }
+      };
+      // O_t (+)= P_t V over the 128 keys in steps of 16
+      auto issue_pv = [&](int t, uint32_t slot, bool accumulate) {
+        const uint32_t dst = tmem + Cfg::col_o(t);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t bd =
+              smem_desc_sw128(sKV + slot * Cfg::kTileBytes + kk * 2048, kBlockBytes, 1024);
+          mma_ts(dst, tmem + Cfg::col_s(t) + kk * 8, bd, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++q_round) {
+        int bh, pair;
+        decode_item(item, a, CAUSAL, bh, pair);
+        const int Jt[2] = {tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL)};
+        const int J = max(Jt[0], Jt[1]);
+        const uint32_t base = kv_it;
+        for (int t = 0; t < 2 && ok; ++t)
+          ok = mbar_wait(smem_u32(&bars->q_full[t]), q_round & 1, abort, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        // K_0
+        {
+          const uint32_t s = base % Cfg::kStages;
+          ok = mbar_wait(smem_u32(&bars->kv_full[s]), (base / Cfg::kStages) & 1, abort, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t) {
+            if (Jt[t] > 0) {
+              issue_s(t, s);
+              mma_commit(smem_u32(&bars->s_full[t]));
+            }
+            if (Jt[t] <= 1) mma_commit(smem_u32(&bars->q_empty[t]));
+          }
+          mma_commit(smem_u32(&bars->kv_empty[s]));
+        }
+        for (int j = 0; j < J && ok; ++j) {
+          const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+          const uint32_t sv = iv % Cfg::kStages, sk = ik % Cfg::kStages;
+          ok = mbar_wait(smem_u32(&bars->kv_full[sv]), (iv / Cfg::kStages) & 1, abort, a.status);
+          if (!ok) break;
+          bool k_ready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= Jt[t]) continue;
+            ok = mbar_wait(smem_u32(&bars->p_full[t]), step[t] & 1, abort, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, sv, j > 0);
+            mma_commit(smem_u32(&bars->o_done[t]));
+            ++step[t];
+            if (j + 1 < Jt[t]) {
+              if (!k_ready) {
+                ok = mbar_wait(smem_u32(&bars->kv_full[sk]), (ik / Cfg::kStages) & 1, abort,
+                               a.status);
+                if (!ok) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(t, sk);
+              mma_commit(smem_u32(&bars->s_full[t]));
+              if (j + 2 == Jt[t]) mma_commit(smem_u32(&bars->q_empty[t]));
+            }
+          }
+          if (!ok) break;
+          mma_commit(smem_u32(&bars->kv_empty[sv]));
+          if (j + 1 < J) {
+            if (!k_ready) {  // K_{j+1} loaded but used by no tile: release it anyway
+              ok = mbar_wait(smem_u32(&bars->kv_full[sk]), (ik / Cfg::kStages) & 1, abort,
+                             a.status);
+              if (!ok) break;
+            }
+            mma_commit(smem_u32(&bars->kv_empty[sk]));
+          }
+        }
+        kv_it = base + 2 * J;
+      }
+      // every MMA issued so far completes before TMEM is released
+      mma_commit(smem_u32(&bars->drain));
+      mbar_drain(smem_u32(&bars->drain), 0, 1000000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;            // query tile of this warpgroup
+    const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
+    const uint32_t t_lane = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
+    const uint32_t tS = t_lane + Cfg::col_s(t);
+    const uint32_t tO = t_lane + Cfg::col_o(t);
+    const float sl2 = a.scale_log2;
+    const float NEG_INF = __int_as_float(0xff800000);
+    uint32_t step = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      int bh, pair;
+      decode_item(item, a, CAUSAL, bh, pair);
+      const int qt = 2 * pair + t;
+      const int J = tile_steps(qt, a, CAUSAL);
+      if (J == 0) continue;
+      float m = NEG_INF, l = 0.f;
+      for (int j = 0; j < J; ++j) {
+        ok = mbar_wait_warp(smem_u32(&bars->s_full[t]), step & 1, abort, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld128(tS, sr);
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        // masks: causal diagonal tile, and keys past N in the last tile
+        int lim = 127;
+        if (CAUSAL && j == qt) lim = r;
+        if (j == a.n_tiles - 1) lim = min(lim, a.N - 1 - j * kTile);
+        const bool masked = lim < 127;
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (c > lim) ? NEG_INF : s[c];
+        }
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        float m_use = m, alpha = 1.f;
+        bool grow = false;
+        if (j == 0) {
+          m_use = mt;
+        } else if ((mt - m) * sl2 > kRescaleTauLog2) {
+          m_use = mt;
+          alpha = ex2_approx((m - mt) * sl2);
+          grow = true;
+        }
+        const float neg = -m_use * sl2;
+        uint32_t pk[64];
+        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float p0 = ex2_approx(fmaf(s[2 * c], sl2, neg));
+          float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, neg));
+          if (masked) {
+            p0 = (2 * c > lim) ? 0.f : p0;
+            p1 = (2 * c + 1 > lim) ? 0.f : p1;
+          }
+          sum[c & 7] += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l = alpha * l + (((sum[0] + sum[1]) + (sum[2] + sum[3])) +
+                         ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+        tmem_st64(tS, pk);
+        if (__any_sync(0xffffffffu, grow)) {
+          // O_t still holds the sum up to tile j-1; PV(j-1) completed before S(j) did
+          ok = mbar_wait_warp(smem_u32(&bars->o_done[t]), (step - 1) & 1, abort, a.status);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            tmem_st32(tO + cc * 32, o);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->p_full[t]));
+        m = m_use;
+        ++step;
+      }
+      if (!ok) break;
+      // epilogue: O / l in bf16 and the log-sum-exp
+      ok = mbar_wait_warp(smem_u32(&bars->o_done[t]), (step - 1) & 1, abort, a.status);
+      if (!ok) break;
+      tc_fence_after();
+      const int row = qt * kTile + r;
+      const bool store = row < a.N;
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.N + row) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
+            dst[v4] = w;
+          }
+        }
+      }
+      if (store)
+        a.lse[static_cast<size_t>(bh) * a.N + row] =
+            fmaf(m, a.scale, lg2_approx(l) * 0.69314718055994531f);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                         const CUtensorMap& mv, const FwdArgs& a, cudaStream_t stream) {
+  constexpr int smem = fwd_smem_bytes<D>();
+  auto kern = fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = min(a.n_items, p.num_sms);
+  kern<<<grid, kFwdThreads, smem, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                       float* lse, cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  CUtensorMap mq, mk, mv;
+  if (!make_tile_map(&mq, q, BH, p.N, p.d) || !make_tile_map(&mk, k, BH, p.N, p.d) ||
+      !make_tile_map(&mv, v, BH, p.N, p.d))
+    return cudaErrorInvalidValue;
+  FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = p.status;
+  a.N = p.N;
+  a.BH = BH;
+  a.n_tiles = (p.N + kTile - 1) / kTile;
+  a.n_pairs = (a.n_tiles + 1) / 2;
+  a.n_items = BH * a.n_pairs;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  if (p.d == 64)
+    return p.causal ? launch_fwd_t<64, true>(p, mq, mk, mv, a, stream)
+                    : launch_fwd_t<64, false>(p, mq, mk, mv, a, stream);
+  return p.causal ? launch_fwd_t<128, true>(p, mq, mk, mv, a, stream)
+                  : launch_fwd_t<128, false>(p, mq, mk, mv, a, stream);
+}
+
+}  // namespace fa

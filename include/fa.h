@@ -1,0 +1,138 @@
+/*
+ * Exact tiled attention on one GB300 (sm_103a): the C ABI of libfa.so.
+ *
+ * O = softmax(scale * Q K^T [+ causal mask]) V, computed tile by tile with an
+ * online softmax so that the N x N score matrix never reaches HBM, plus the
+ * recomputing backward that yields dQ, dK and dV.
+ *
+ * Sources for what is computed (pages on FlashAttention-2):
+ *  - "flashattention-2" glossary: "How FlashAttention-2 Works (Tiled
+ *    Algorithm)" table (Q tile loaded once, K/V tiles streamed, S = Q K^T,
+ *    online softmax, O accumulated, written once) and the "Performance
+ *    Comparison" table (the result is exact; memory O(N)).
+ *  - "Flash Attention v2" notes: "Detailed Algorithm Comparison", forward
+ *    pass (running max m, running sum l, rescale factor exp(m - m_new), the
+ *    statistics kept for the backward) and "Backward Pass Computation"
+ *    (recompute S and P per block, then dP, dQ, dK, dV).
+ *  - "FlashAttention-2 paper" digest: "Three changes" (deferred rescaling,
+ *    query blocks split across thread blocks even within one head).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors q, k, v, o, dO, dq, dk, dv are bf16, shape [B, H, N, d],
+ *    contiguous, d innermost. lse is fp32 [B, H, N] (natural log).
+ *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned. The library keeps no reference to them after the call.
+ *  - d must be 64 or 128; B, H, N >= 1; B*H < 2^31 (offsets are computed in
+ *    64 bits, so a tensor may hold more than 2^31 elements).
+ *  - Causal masking is top-left aligned with equal query and key lengths:
+ *    query i sees keys j <= i. scale must be finite and >= 0.
+ *  - stream is a cudaStream_t (NULL = the legacy default stream). Every call
+ *    only enqueues work and returns; outputs are valid once the stream has
+ *    reached that point. No call synchronises the device.
+ *  - Argument errors are reported before anything is enqueued, and the
+ *    outputs are then untouched. Launch failures return FA_ERR_CUDA.
+ *  - A kernel that waits on an on-chip barrier for longer than 2 s gives up,
+ *    leaves the GPU usable and records FA_ERR_TIMEOUT in a device status word
+ *    shared by all calls of the process; fa_last_device_status() reads it.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, size < 1, bad scale */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 or 128, too large */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+  FA_ERR_TIMEOUT = 4,     /* a device-side bounded wait expired */
+  FA_ERR_WORKSPACE = 5    /* backward workspace null or too small */
+} fa_status;
+
+/* Version of this ABI; bumped on any incompatible change. */
+int fa_abi_version(void);
+
+/*
+ * Forward. Writes o = softmax(scale * q k^T [masked]) v in bf16 and
+ * lse[b,h,i] = ln sum_j exp(scale * q_i . k_j) over the visible keys, in fp32.
+ * ("flashattention-2" glossary, "How FlashAttention-2 Works (Tiled
+ * Algorithm)", steps 1-7; "Flash Attention v2" notes, "Detailed Algorithm
+ * Comparison", forward pass, with the final division by the row sum and the
+ * statistics stored for the backward as one log-sum-exp per row.)
+ * q, k, v: inputs; o, lse: outputs, fully overwritten (rows 0..N-1).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Size in bytes of the device workspace fa_bwd needs for these sizes: an
+ * fp32 [B,H,N] row term D and an fp32 [B,H,N,d] dQ accumulator. Returns 0
+ * for arguments fa_bwd would reject.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward of the loss sum(o * dO). Recomputes S and P per tile from q, k and
+ * the forward's lse ("Flash Attention v2" notes, "Backward Pass
+ * Computation": recompute S block by block, then dP, dQ, dK, dV) with the
+ * full softmax Jacobian:
+ *   D_i = sum_c dO_ic o_ic,  P_ij = exp(scale q_i.k_j - lse_i),
+ *   dS_ij = P_ij (dO_i.v_j - D_i),
+ *   dq = scale dS k,  dk = scale dS^T q,  dv = P^T dO.
+ * q, k, v, o, lse, dO: inputs (o and lse as written by fa_fwd with the same
+ * arguments). dq, dk, dv: outputs, fully overwritten. workspace: device
+ * memory of at least fa_bwd_workspace_size() bytes, 16-byte aligned, owned by
+ * the caller, clobbered by the call (its contents on entry do not matter).
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages fa_bwd runs, in this order, for callers that schedule or
+ * time them separately. Arguments as for fa_bwd; the same workspace must be
+ * passed to all three, and the stages of one backward must not overlap with
+ * another call that uses that workspace.
+ *  1. fa_bwd_preprocess: D_i = sum_c dO_ic o_ic, the lse rows in log2 units,
+ *     and zeroes the fp32 dQ accumulator (all in the workspace).
+ *  2. fa_bwd_dkdv: for every key block, loops over the query blocks,
+ *     recomputes S and P, writes dk and dv, and adds each block's
+ *     contribution dS K to the dQ accumulator.
+ *  3. fa_bwd_dq_finalize: dq = bf16(scale * dQ accumulator).
+ */
+fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dO, int B, int H, int N,
+                            int d, void* workspace, size_t workspace_bytes, void* stream);
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                      void* dv, int B, int H, int N, int d, int causal, float scale,
+                      void* workspace, size_t workspace_bytes, void* stream);
+fa_status fa_bwd_dq_finalize(void* dq, int B, int H, int N, int d, float scale, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
+ * Self-test of the failure path (no counterpart in the method): enqueues a
+ * one-thread kernel that waits on an on-chip barrier nothing ever arrives on,
+ * with a limit of limit_ms milliseconds (1..2000) instead of the 2 s the
+ * attention kernels use. The wait gives up and records FA_ERR_TIMEOUT, which
+ * the next fa_last_device_status() returns; the GPU context stays usable.
+ */
+fa_status fa_selftest_wait_timeout(int limit_ms, void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * Synchronises the stream, then returns FA_ERR_TIMEOUT if any kernel of this
+ * process has recorded a bounded-wait timeout since the last call (and clears
+ * the record), FA_ERR_CUDA if the synchronisation failed, else FA_OK.
+ */
+fa_status fa_last_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,120 @@
+"""The C ABI on the host: the library loads, exports every function that
+include/fa.h declares, and rejects bad arguments before launching anything.
+No call here reaches a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_28_gb300 as fa
+from exact_tiled_attention_28_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.library_path()):
+        from exact_tiled_attention_28_gb300 import build
+        build.build()
+    return fa.load()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(fa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    decl = declared_functions()
+    assert "fa_fwd" in decl and "fa_bwd" in decl
+    for name in decl:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert set(decl) <= set(binding.EXPORTED)
+
+
+def test_abi_version(lib):
+    assert lib.fa_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = fa.fa_status_string(code)
+        assert s.startswith("FA_")
+    assert "unknown" in fa.fa_status_string(99)
+
+
+P = 4096  # a 16-byte-aligned fake address: never dereferenced, the calls fail first
+
+
+def fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return binding.fa_fwd_raw(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+def bwd(lib, ws=P, ws_bytes=None, B=1, H=1, N=128, d=64, scale=0.125, null=None):
+    ptrs = [P] * 9
+    if null is not None:
+        ptrs[null] = None
+    if ws_bytes is None:
+        ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    return binding.fa_bwd_raw(*ptrs, B, H, N, d, 0, scale, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=P + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=65536, H=32768), fa.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_before_launch(lib, kw, want):
+    assert fwd(lib, **kw) == want
+
+
+def test_bwd_rejects_before_launch(lib):
+    for i in range(9):
+        assert bwd(lib, null=i) == fa.FA_ERR_INVALID_ARG
+    assert bwd(lib, d=32) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(lib, ws=None) == fa.FA_ERR_WORKSPACE
+    assert bwd(lib, ws=P + 4) == fa.FA_ERR_WORKSPACE
+    assert bwd(lib, ws_bytes=fa.fa_bwd_workspace_size(1, 1, 128, 64) - 1) == fa.FA_ERR_WORKSPACE
+
+
+def test_workspace_size(lib):
+    for B, H, N, d in ((1, 1, 1, 64), (4, 8, 1024, 64), (1, 16, 32768, 128), (2, 3, 77, 128)):
+        assert fa.fa_bwd_workspace_size(B, H, N, d) >= 4 * B * H * N * (d + 1)
+    assert fa.fa_bwd_workspace_size(1, 1, 0, 64) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 16, 80) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without the shared library every call raises."""
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "libfa.so"))
+    with pytest.raises(fa.FaError):
+        binding.load()
+    with pytest.raises(fa.FaError):
+        fa.fa_bwd_workspace_size(1, 1, 128, 64)
+
+
+def test_library_has_no_torch_dependency(lib):
+    """The C ABI takes plain pointers: the shared object links no torch library."""
+    path = fa.library_path()
+    data = open(path, "rb").read()
+    assert b"libtorch" not in data and b"libc10" not in data
+    assert isinstance(lib, ctypes.CDLL)
