@@ -209,7 +209,7 @@ def run_ours(args):
     import torch
 
     import exact_tiled_attention_28_gb300 as fa
-    from exact_tiled_attention_28_gb300 import inputs
+    from exact_tiled_attention_28_gb300 import inputs, replicas
 
     world, rank, local = dist_setup(args)
     if world > 1:
@@ -223,7 +223,7 @@ def run_ours(args):
     B, H, N, d = WORKLOADS[args.workload]
     causal = bool(args.causal)
     scale = 1.0 / math.sqrt(d)
-    seed = 1000 + rank
+    seed = replicas.replica_seed(1000, rank)
 
     bits = inputs.attention_inputs(seed, B, H, N, d)
     host = {n: inputs.bits_to_torch_bf16(b).pin_memory() for n, b in bits.items()}
@@ -279,12 +279,7 @@ def run_ours(args):
     bwd_ms = statistics.mean(e[2].elapsed_time(e[5]) for e in evs)
     ms_step = ms_total / args.steps
 
-    if world > 1:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step_max = float(t.item())
-    else:
-        ms_step_max = ms_step
+    ms_step_max = replicas.max_over_ranks(ms_step, dev)
 
     # end to end through host buffers: pinned inputs in, every output back
     out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
@@ -308,7 +303,7 @@ def run_ours(args):
     F = fwd_flops(B, H, N, d, causal)
     peaks = load_peaks()
     tag = "of " + peaks["source"]
-    value = world * 3.5 * F / (ms_step_max * 1e-3) / 1e12
+    value = replicas.aggregate_throughput(3.5 * F, world, ms_step_max)
     dkdv_tf = 2.5 * F / (dkdv_ms * 1e-3) / 1e12
     fwd_tf = F / (fwd_ms * 1e-3) / 1e12
     traffic = NCU_TRAFFIC_BYTES.get((args.workload, causal))
