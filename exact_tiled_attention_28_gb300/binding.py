@@ -23,8 +23,11 @@ FA_ERR_WORKSPACE = 5
 
 # every symbol include/fa.h declares
 EXPORTED = ("fa_abi_version", "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess",
-            "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_selftest_wait_timeout", "fa_status_string",
-            "fa_last_device_status")
+            "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout",
+            "fa_status_string", "fa_last_device_status")
+
+# fixed device scratch of fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in include/fa.h)
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lib = None
 
@@ -63,6 +66,8 @@ def load():
     lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.fa_bwd_dq_finalize.restype = i
     lib.fa_bwd_dq_finalize.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -141,6 +146,12 @@ def fa_bwd_dq_finalize_raw(dq, B, H, N, d, scale, workspace, workspace_bytes, st
                                      stream)
 
 
+def fa_bwd_noalloc_raw(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, causal, scale,
+                       stream) -> int:
+    return load().fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, int(bool(causal)),
+                                 float(scale), stream)
+
+
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_size(B, H, N, d))
 
@@ -212,3 +223,21 @@ def fa_bwd_stages(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, w
     _check(fa_bwd_dq_finalize_raw(P["dq"], B, H, N, d, scale, ws, nws, st), "fa_bwd_dq_finalize")
     if events:
         events[3].record(s)
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float,
+                   stream=None) -> None:
+    """fa_bwd without a workspace argument: the library's fixed device scratch
+    array is used, nothing is allocated. For callers that cannot allocate
+    device memory; sizes whose workspace exceeds NOALLOC_SCRATCH_BYTES raise
+    (FA_ERR_WORKSPACE). Calls overlapping on the GPU race on the shared array."""
+    import torch
+    B, H, N, d = _shape(q)
+    bf = torch.bfloat16
+    ptrs = [_dev_ptr(t, n, bf, (B, H, N, d))
+            for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
+    ptrs.append(_dev_ptr(lse, "lse", torch.float32, (B, H, N)))
+    ptrs += [_dev_ptr(t, n, bf, (B, H, N, d))
+             for t, n in ((do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))]
+    _check(fa_bwd_noalloc_raw(*ptrs, B, H, N, d, causal, scale, _stream_handle(stream)),
+           "fa_bwd_noalloc")

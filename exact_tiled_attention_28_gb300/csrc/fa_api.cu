@@ -91,6 +91,16 @@ __global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
 
 }  // namespace
 
+// Device facts for launchers outside this file (the no-alloc entry point).
+cudaError_t current_device_setup(int* num_sms, int** status) {
+  DeviceInfo di;
+  const cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  *num_sms = di.num_sms;
+  *status = di.status;
+  return cudaSuccess;
+}
+
 bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
   if (!g_encode) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),

@@ -121,6 +121,31 @@ fa_status fa_bwd_dq_finalize(void* dq, int B, int H, int N, int d, float scale, 
  */
 fa_status fa_selftest_wait_timeout(int limit_ms, void* stream);
 
+/*
+ * Backward without any allocation, for callers that cannot allocate device
+ * memory: code whose device memory all belongs to its own pool, or code that
+ * must not call cudaMalloc while running because cudaMalloc can synchronise
+ * the device and take unbounded time. The paper has no counterpart; this is a
+ * deployment variant of fa_bwd.
+ *
+ * Same arguments, results and errors as fa_bwd, minus the workspace: the
+ * library uses a fixed device array of FA_NOALLOC_SCRATCH_BYTES instead,
+ * which every GPU that loads libfa.so holds until the process exits. Sizes
+ * whose fa_bwd_workspace_size() exceeds that return FA_ERR_WORKSPACE before
+ * anything is enqueued (e.g. B*H*N*(d+2) fp32 values must fit in 32 MiB).
+ * The call allocates nothing and calls no allocating routine. The first call
+ * on each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents; the
+ * call itself rewrites every part it reads, so nothing needs clearing. Calls
+ * that overlap on the GPU (different streams or host threads) race on the
+ * array and give wrong results: run them one after another.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, int causal, float scale, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(int status);
 
