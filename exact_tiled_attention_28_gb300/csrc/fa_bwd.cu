@@ -17,15 +17,22 @@
 //     keeps K_j and V_j in shared memory and dV_j, dK_j in tensor memory and
 //     loops over the query blocks i (causal: i >= j, longest blocks first):
 //       S^T = K_j Q_i^T and dP^T = V_j dO_i^T       (tcgen05, SS)
-//       P^T, dS^T by the compute warps, one thread per key row  (TMEM <-> regs)
+//       P^T, dS^T by two compute warpgroups, one thread per key row, each
+//       warpgroup owning 64 of the 128 query columns  (TMEM <-> regs)
 //       dV += P^T dO_i and dK += dS^T Q_i           (tcgen05, A from TMEM)
-//       dQ_i = dS K_j                               (tcgen05, A = dS^T in SMEM)
+//       d = 128: dQ_i^T = K_j^T dS^T                (tcgen05, both from SMEM)
+//       d = 64:  dQ_i = dS K_j                      (tcgen05, both from SMEM)
 //     and four more warps read dQ_i out of TMEM and add it to the fp32
-//     accumulator in global memory (vector atomics).
+//     accumulator in global memory. With dQ^T in TMEM (lanes = head dim,
+//     columns = queries) a warp's 32 atomics cover one contiguous 128-byte
+//     row segment.
 //  3. dq_convert_kernel: dq = bf16(scale * accumulator).
 //
-// TMEM (512 columns): S^T/P^T [0,128), dP^T/dS^T then dQ_i [128,256),
-// dV [256, 256+d), dK [256+d, 256+2d).
+// TMEM (512 columns): S^T [0,128), dP^T then dQ_i [128,256), dV [256, 256+d),
+// dK [256+d, 256+2d). Compute warpgroup c reads columns 64c..64c+63 of S^T and
+// dP^T and writes its packed bf16 P^T / dS^T (two per column) over the first 32
+// of those same columns, so neither warpgroup overwrites a column the other
+// still has to read; the MMAs address the two 32-column halves separately.
 
 #include <algorithm>
 
@@ -37,9 +44,10 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 320;  // 4 compute warps, 4 dQ warps, load warp, MMA warp
-constexpr int kBwdLoadWarp = 8;
-constexpr int kBwdMmaWarp = 9;
+constexpr int kBwdThreads = 448;  // 8 compute warps, 4 dQ warps, load warp, MMA warp
+constexpr int kBwdDqWarp0 = 8;
+constexpr int kBwdLoadWarp = 12;
+constexpr int kBwdMmaWarp = 13;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr int kBlk = kTile * 64 * 2;  // 16 KiB: one 128-row x 64-column bf16 block
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;
@@ -178,6 +186,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 448 threads: four warps on some SM sub-partitions, whose 16384-register
+// files then allow 128 registers per thread
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -210,8 +220,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->dp_full), 1);
-    mbar_init(smem_u32(&bars->p_ready), 128);
-    mbar_init(smem_u32(&bars->ds_ready), 128);
+    mbar_init(smem_u32(&bars->p_ready), 256);
+    mbar_init(smem_u32(&bars->ds_ready), 256);
     mbar_init(smem_u32(&bars->dq_full), 1);
     mbar_init(smem_u32(&bars->dq_free), 128);
     mbar_init(smem_u32(&bars->acc_done), 1);
@@ -294,8 +304,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_kq = idesc_bf16_f32(kTile, kTile, false, false);
       // dV += P^T dO, dK += dS^T Q: A from TMEM, B MN-major, N = d
       constexpr uint32_t idesc_acc = idesc_bf16_f32(kTile, D, false, true);
-      // dQ = dS K: A = dS^T in SMEM (MN-major), B = K MN-major, N = d
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(kTile, D, true, true);
+      // d = 128: dQ^T = K^T dS^T (M = d, N = 128 queries); d = 64: dQ = dS K
+      // (M = 128 queries, N = d). Both operands MN-major in SMEM.
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(kTile, D == 128 ? kTile : D, true, true);
       uint32_t st_it = 0, kv_round = 0, it = 0;
       bool ok = true;
 
@@ -307,17 +318,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  smem_desc_sw128(b_tile + off, 16, 1024), idesc_kq, kk > 0);
         }
       };
-      auto issue_acc = [&](uint32_t dst, uint32_t a_tmem, uint32_t b_tile, bool accumulate) {
+      // A = packed P^T or dS^T: queries 16kk..16kk+15 sit in the half of the
+      // region written by compute warpgroup kk / 4, at column 64 (kk/4) + 8 (kk%4)
+      auto issue_acc = [&](uint32_t dst, uint32_t a_region, uint32_t b_tile, bool accumulate) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(dst, a_tmem + kk * 8, smem_desc_sw128(b_tile + kk * 2048, kBlk, 1024), idesc_acc,
+          mma_ts(dst, a_region + 64 * (kk >> 2) + 8 * (kk & 3),
+                 smem_desc_sw128(b_tile + kk * 2048, kBlk, 1024), idesc_acc,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
       auto issue_dq = [&]() {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tmem + kColDP, smem_desc_sw128(sDS + kk * 2048, kBlk, 1024),
-                 smem_desc_sw128(sK + kk * 2048, kBlk, 1024), idesc_dq, kk > 0);
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t ds_desc = smem_desc_sw128(sDS + kk * 2048, kBlk, 1024);
+          const uint64_t k_desc = smem_desc_sw128(sK + kk * 2048, kBlk, 1024);
+          if constexpr (D == 128)
+            mma_ss(tmem + kColDP, k_desc, ds_desc, idesc_dq, kk > 0);
+          else
+            mma_ss(tmem + kColDP, ds_desc, k_desc, idesc_dq, kk > 0);
+        }
       };
 
       for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++kv_round) {
@@ -382,15 +401,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(smem_u32(&bars->drain));
       mbar_drain(smem_u32(&bars->drain), 0, 1000000000ull);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------ compute warps: P^T and dS^T
-    const int r = warp * 32 + lane;  // key row within the block = TMEM lane
-    const uint32_t t_lane = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
+  } else if (warp < 8) {
+    // -------------------------------- compute warps: P^T and dS^T, 64 queries each
+    const int wg = warp >> 2;            // query columns 64 wg .. 64 wg + 63
+    const int r = (warp & 3) * 32 + lane;  // key row within the block = TMEM lane
+    const uint32_t t_lane = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
+    const uint32_t tS = t_lane + kColS + 64 * wg;
+    const uint32_t tDP = t_lane + kColDP + 64 * wg;
     const float sl2 = a.scale_log2;
     uint32_t st_it = 0, it = 0, kv_round = 0;
     bool ok = true;
-    // swizzled row of dS^T in shared memory: 128-byte rows, 16-byte chunks XOR (row & 7)
-    const uint32_t ds_row = sDS + r * 128;
+    // row r of query block wg of dS^T in shared memory: 128-byte rows, 16-byte
+    // chunks stored at chunk ^ (r & 7)
+    const uint32_t ds_row = sDS + wg * kBlk + r * 128;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++kv_round) {
       int bh, j;
       decode_kv_item(item, a, CAUSAL, bh, j);
@@ -400,57 +423,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int i = i0 + u;
         const uint32_t s = st_it % Cfg::kStages;
         const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kOffStages +
-                                                           s * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
+                                                           s * Cfg::kStageBytes +
+                                                           2 * Cfg::kTileBytes) + 64 * wg;
         const float* Dq = lse2 + 128;
         // phase A: P^T = exp2(S^T * scale*log2e - lse2[q]), causal mask on the diagonal
         ok = mbar_wait_warp(smem_u32(&bars->s_full), it & 1, abort, a.status);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld128(t_lane + kColS, sr);
+        uint32_t sr[64];
+        tmem_ld64(tS, sr);
         const bool diag = CAUSAL && i == j;
-        uint32_t pk[64];
+        const int qlo = 64 * wg;
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 2 * c);
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -l2.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -l2.y));
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                                 make_float2(sl2, sl2), make_float2(-l2.x, -l2.y));
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
           if (diag) {  // query q sees key r only if r <= q
-            p0 = (2 * c < r) ? 0.f : p0;
-            p1 = (2 * c + 1 < r) ? 0.f : p1;
+            p0 = (qlo + 2 * c < r) ? 0.f : p0;
+            p1 = (qlo + 2 * c + 1 < r) ? 0.f : p1;
           }
           pk[c] = pack_bf16x2(p0, p1);
         }
-        tmem_st64(t_lane + kColS, pk);
+        tmem_st32(tS, pk);
         tc_fence_before();
         mbar_arrive(smem_u32(&bars->p_ready));
-        // phase B: dS^T = P^T o (dP^T - D[q]); needs the previous dQ MMA done
-        // with the dS buffer (its completion precedes dP^T(i) in MMA order)
+        // phase B: dS^T = P^T o (dP^T - D[q]); the previous dQ MMA is done with
+        // the dS buffer (its completion precedes dP^T(i) in MMA order)
         ok = mbar_wait_warp(smem_u32(&bars->dp_full), it & 1, abort, a.status);
         if (!ok) break;
         tc_fence_after();
-        // 32 queries at a time: dP^T chunk in, dS^T chunk out to TMEM and SMEM
+        // two chunks of 32 queries: dP^T in, dS^T out to TMEM and shared memory
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < 2; ++h) {
           uint32_t dp[32];
-          tmem_ld32(t_lane + kColDP + 32 * h, dp);
+          tmem_ld32(tDP + 32 * h, dp);
           uint32_t ds[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const int q = 32 * h + 2 * c;
             const float2 pf =
                 __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[16 * h + c]));
-            const float2 dd = *reinterpret_cast<const float2*>(Dq + q);
-            ds[c] = pack_bf16x2(pf.x * (__uint_as_float(dp[2 * c]) - dd.x),
-                                pf.y * (__uint_as_float(dp[2 * c + 1]) - dd.y));
+            const float2 dd = *reinterpret_cast<const float2*>(Dq + 32 * h + 2 * c);
+            const float2 g = fadd2(make_float2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1])),
+                                   make_float2(-dd.x, -dd.y));
+            const float2 v = fmul2(pf, g);
+            ds[c] = pack_bf16x2(v.x, v.y);
           }
-          tmem_st16(t_lane + kColDP + 16 * h, ds);
-          // dS^T row r, queries 32h..32h+31: query block cb = h / 2, 16-byte
-          // chunks ch = 4 (h % 2) .. +3, stored at chunk ch ^ (r & 7)
+          tmem_st16(tDP + 16 * h, ds);
 #pragma unroll
           for (int u4 = 0; u4 < 4; ++u4) {
-            const int ch = 4 * (h & 1) + u4;
-            const uint32_t addr = ds_row + (h >> 1) * kBlk + ((ch ^ (r & 7)) << 4);
+            const int ch = 4 * h + u4;
+            const uint32_t addr = ds_row + ((ch ^ (r & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(ds[4 * u4]),
                          "r"(ds[4 * u4 + 1]), "r"(ds[4 * u4 + 2]), "r"(ds[4 * u4 + 3])
                          : "memory");
@@ -461,76 +487,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(smem_u32(&bars->ds_ready));
       }
       if (!ok) break;
-      // epilogue: dV and scale * dK of this key block
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
       ok = mbar_wait_warp(smem_u32(&bars->acc_done), kv_round & 1, abort, a.status);
       if (!ok) break;
       tc_fence_after();
       const int key = j * kTile + r;
       const bool store = key < a.N;
       const size_t base = (static_cast<size_t>(bh) * a.N + key) * D;
+      __nv_bfloat16* out = (wg == 0 ? a.dv : a.dk) + base;
+      const float mul = wg == 0 ? 1.f : a.scale;
+      const uint32_t col = wg == 0 ? kColDV : Cfg::col_dk();
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* out = (which == 0 ? a.dv : a.dk) + base;
-        const float mul = which == 0 ? 1.f : a.scale;
-        const uint32_t col = which == 0 ? kColDV : Cfg::col_dk();
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(t_lane + col + cc * 32, v);
-          if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(out + cc * 32);
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(t_lane + col + cc * 32, v);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(out + cc * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-              w.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-              w.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-              w.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
-              dst[v4] = w;
-            }
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+            w.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+            w.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+            w.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+            dst[v4] = w;
           }
         }
       }
       // the next item's first dV/dK MMAs overwrite these accumulators only
-      // after p_ready/ds_ready of that item, which this warpgroup signals later
+      // after p_ready/ds_ready of that item, which these warps signal later
     }
   } else {
     // ------------------------------------------------- dQ warps: add dQ_i
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // query row within the block
-    const uint32_t t_lane = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
-    uint32_t it = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
-      int bh, j;
-      decode_kv_item(item, a, CAUSAL, bh, j);
-      const int i0 = CAUSAL ? j : 0;
-      for (int i = i0; i < n_q; ++i, ++it) {
-        ok = mbar_wait_warp(smem_u32(&bars->dq_full), it & 1, abort, a.status);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t v[D];
-        if constexpr (D == 128) {
-          tmem_ld128(t_lane + kColDP, v);
-        } else {
-          uint32_t t32[32];
-          tmem_ld32(t_lane + kColDP, t32);
+    if (warp >= kBwdDqWarp0 && warp < kBwdDqWarp0 + 4) {
+      const int wq = warp & 3;
+      const uint32_t t_lane = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+        int bh, j;
+        decode_kv_item(item, a, CAUSAL, bh, j);
+        const int i0 = CAUSAL ? j : 0;
+        for (int i = i0; i < n_q; ++i, ++it) {
+          ok = mbar_wait_warp(smem_u32(&bars->dq_full), it & 1, abort, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          if constexpr (D == 128) {
+            // lane = head-dim index dd, columns = the 128 queries of block i
+            // two halves of 64 queries (128 registers per thread at most); TMEM is
+            // released once the second half is in registers
+            const int dd = wq * 32 + lane;
+            const int rows = min(kTile, a.N - i * kTile);
+            float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile) * D + dd;
+            uint32_t v[64];
+            tmem_ld64(t_lane + kColDP, v);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = t32[c];
-          tmem_ld32(t_lane + kColDP + 32, t32);
+            for (int q = 0; q < 64; ++q)
+              if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
+            tmem_ld64(t_lane + kColDP + 64, v);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->dq_free));
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[32 + c] = t32[c];
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars->dq_free));
-        const int row = i * kTile + r;
-        if (row < a.N) {
-          float4* dst = reinterpret_cast<float4*>(a.dq_acc + (static_cast<size_t>(bh) * a.N + row) * D);
+            for (int q = 0; q < 64; ++q)
+              if (64 + q < rows) atomicAdd(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(v[q]));
+          } else {
+            // lane = query row, columns = the d = 64 head-dim values
+            uint32_t v[64];
+            tmem_ld64(t_lane + kColDP, v);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->dq_free));
+            const int row = i * kTile + wq * 32 + lane;
+            if (row < a.N) {
+              float4* dst = reinterpret_cast<float4*>(a.dq_acc + (static_cast<size_t>(bh) * a.N + row) * D);
 #pragma unroll
-          for (int c = 0; c < D / 4; ++c)
-            atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                           __uint_as_float(v[4 * c + 2]),
-                                           __uint_as_float(v[4 * c + 3])));
+              for (int c = 0; c < D / 4; ++c)
+                atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                               __uint_as_float(v[4 * c + 2]),
+                                               __uint_as_float(v[4 * c + 3])));
+            }
+          }
         }
       }
     }

@@ -157,7 +157,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int bh, pair;
         decode_item(item, a, CAUSAL, bh, pair);
         const int J = max(tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL));
-        for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
           ok = mbar_wait(smem_u32(&bars->q_empty[t]), (q_issued[t] & 1) ^ 1, abort, a.status);
           if (!ok) break;
           const uint32_t bar = smem_u32(&bars->q_full[t]);
@@ -235,8 +237,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int Jt[2] = {tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL)};
         const int J = max(Jt[0], Jt[1]);
         const uint32_t base = kv_it;
-        for (int t = 0; t < 2 && ok; ++t)
-          ok = mbar_wait(smem_u32(&bars->q_full[t]), q_round & 1, abort, a.status);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ok) ok = mbar_wait(smem_u32(&bars->q_full[t]), q_round & 1, abort, a.status);
         if (!ok) break;
         tc_fence_after();
         // K_0
@@ -245,6 +248,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ok = mbar_wait(smem_u32(&bars->kv_full[s]), (base / Cfg::kStages) & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (Jt[t] > 0) {
               issue_s(t, s);
@@ -260,8 +264,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ok = mbar_wait(smem_u32(&bars->kv_full[sv]), (iv / Cfg::kStages) & 1, abort, a.status);
           if (!ok) break;
           bool k_ready = false;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= Jt[t]) continue;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || j >= Jt[t]) continue;
             ok = mbar_wait(smem_u32(&bars->p_full[t]), step[t] & 1, abort, a.status);
             if (!ok) break;
             tc_fence_after();
@@ -334,13 +339,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c > lim) ? NEG_INF : s[c];
         }
+        // row max: 8 independent chains of 3-input max
         float mx[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = s[u];
+        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(s[u], s[u + 8]);
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = fmax3(mx[u], s[c + u], s[c + 8 + u]);
+        }
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7]));
         float m_use = m, alpha = 1.f;
         bool grow = false;
         if (j == 0) {
@@ -350,22 +359,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           alpha = ex2_approx((m - mt) * sl2);
           grow = true;
         }
-        const float neg = -m_use * sl2;
+        // p = 2^(s * scale*log2e - m * scale*log2e), two lanes per instruction
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 negv = make_float2(-m_use * sl2, -m_use * sl2);
         uint32_t pk[64];
-        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          float p0 = ex2_approx(fmaf(s[2 * c], sl2, neg));
-          float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, neg));
+          const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2v, negv);
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
           if (masked) {
             p0 = (2 * c > lim) ? 0.f : p0;
             p1 = (2 * c + 1 > lim) ? 0.f : p1;
           }
-          sum[c & 7] += p0 + p1;
+          acc[c & 3] = fadd2(acc[c & 3], make_float2(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
-        l = alpha * l + (((sum[0] + sum[1]) + (sum[2] + sum[3])) +
-                         ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+        const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+        const float2 a03 = fadd2(a01, a23);
+        l = alpha * l + (a03.x + a03.y);
         tmem_st64(tS, pk);
         if (__any_sync(0xffffffffu, grow)) {
           // O_t still holds the sum up to tile j-1; PV(j-1) completed before S(j) did
