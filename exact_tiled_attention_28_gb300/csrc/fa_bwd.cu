@@ -173,6 +173,16 @@ __device__ __forceinline__ void decode_kv_item(int item, const BwdArgs& a, bool 
   }
 }
 
+// The u-th query block visited by key block j. Causal: j, j+1, ..., n_q-1.
+// Non-causal: all blocks, starting at j and wrapping around, so that the CTAs
+// working on neighbouring key blocks of one head at the same time add into
+// different dQ rows instead of contending for the same ones.
+__device__ __forceinline__ int qblock_at(int j, int u, int n_q, bool causal) {
+  if (causal) return j + u;
+  const int i = j + u;
+  return i < n_q ? i : i - n_q;
+}
+
 __device__ __forceinline__ void cp_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                             uint32_t bar) {
   asm volatile(
@@ -220,10 +230,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->dp_full), 1);
-    mbar_init(smem_u32(&bars->p_ready), 256);
-    mbar_init(smem_u32(&bars->ds_ready), 256);
+    mbar_init(smem_u32(&bars->p_ready), 8);   // one elected lane per compute warp
+    mbar_init(smem_u32(&bars->ds_ready), 8);
     mbar_init(smem_u32(&bars->dq_full), 1);
-    mbar_init(smem_u32(&bars->dq_free), 128);
+    mbar_init(smem_u32(&bars->dq_free), 4);   // one elected lane per dQ warp
     mbar_init(smem_u32(&bars->acc_done), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
@@ -265,7 +275,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           ++kv_round;
         }
-        for (int i = CAUSAL ? j : 0; i < n_q && ok; ++i) {
+        const int n_it = CAUSAL ? n_q - j : n_q;
+        for (int u = 0; u < n_it && ok; ++u) {
+          const int i = qblock_at(j, u, n_q, CAUSAL);
           const uint32_t s = st_it % Cfg::kStages;
           ok = mbar_wait(smem_u32(&bars->st_empty[s]), ((st_it / Cfg::kStages) & 1) ^ 1, abort,
                          a.status);
@@ -310,28 +322,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t st_it = 0, kv_round = 0, it = 0;
       bool ok = true;
 
+      // descriptors are built once per tile; a K step adds a constant
       auto issue_kq = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile) {
+        const SmemDesc da = make_desc_sw128(a_tile, 16, 1024);
+        const SmemDesc db = make_desc_sw128(b_tile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
-          mma_ss(dst, smem_desc_sw128(a_tile + off, 16, 1024),
-                 smem_desc_sw128(b_tile + off, 16, 1024), idesc_kq, kk > 0);
+          mma_ss(dst, desc_at(da, off), desc_at(db, off), idesc_kq, kk > 0);
         }
       };
       // A = packed P^T or dS^T: queries 16kk..16kk+15 sit in the half of the
       // region written by compute warpgroup kk / 4, at column 64 (kk/4) + 8 (kk%4)
       auto issue_acc = [&](uint32_t dst, uint32_t a_region, uint32_t b_tile, bool accumulate) {
+        const SmemDesc db = make_desc_sw128(b_tile, kBlk, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(dst, a_region + 64 * (kk >> 2) + 8 * (kk & 3),
-                 smem_desc_sw128(b_tile + kk * 2048, kBlk, 1024), idesc_acc,
+          mma_ts(dst, a_region + 64 * (kk >> 2) + 8 * (kk & 3), desc_at(db, kk * 2048), idesc_acc,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
+      const SmemDesc d_ds = make_desc_sw128(sDS, kBlk, 1024);
+      const SmemDesc d_kmn = make_desc_sw128(sK, kBlk, 1024);
       auto issue_dq = [&]() {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t ds_desc = smem_desc_sw128(sDS + kk * 2048, kBlk, 1024);
-          const uint64_t k_desc = smem_desc_sw128(sK + kk * 2048, kBlk, 1024);
+          const uint64_t ds_desc = desc_at(d_ds, kk * 2048);
+          const uint64_t k_desc = desc_at(d_kmn, kk * 2048);
           if constexpr (D == 128)
             mma_ss(tmem + kColDP, k_desc, ds_desc, idesc_dq, kk > 0);
           else
@@ -420,7 +436,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int i0 = CAUSAL ? j : 0;
       const int n_it = n_q - i0;
       for (int u = 0; u < n_it; ++u, ++it, ++st_it) {
-        const int i = i0 + u;
+        const int i = qblock_at(j, u, n_q, CAUSAL);
         const uint32_t s = st_it % Cfg::kStages;
         const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kOffStages +
                                                            s * Cfg::kStageBytes +
@@ -450,7 +466,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tmem_st32(tS, pk);
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars->p_ready));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));
         // phase B: dS^T = P^T o (dP^T - D[q]); the previous dQ MMA is done with
         // the dS buffer (its completion precedes dP^T(i) in MMA order)
         ok = mbar_wait_warp(smem_u32(&bars->dp_full), it & 1, abort, a.status);
@@ -484,7 +501,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars->ds_ready));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
       }
       if (!ok) break;
       // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
@@ -527,8 +545,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
-        const int i0 = CAUSAL ? j : 0;
-        for (int i = i0; i < n_q; ++i, ++it) {
+        const int n_it = CAUSAL ? n_q - j : n_q;
+        for (int u = 0; u < n_it; ++u, ++it) {
+          const int i = qblock_at(j, u, n_q, CAUSAL);
           ok = mbar_wait_warp(smem_u32(&bars->dq_full), it & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
@@ -546,7 +565,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
             tmem_ld64(t_lane + kColDP + 64, v);
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars->dq_free));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
 #pragma unroll
             for (int q = 0; q < 64; ++q)
               if (64 + q < rows) atomicAdd(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(v[q]));
@@ -555,7 +575,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t v[64];
             tmem_ld64(t_lane + kColDP, v);
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars->dq_free));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
             const int row = i * kTile + wq * 32 + lane;
             if (row < a.N) {
               float4* dst = reinterpret_cast<float4*>(a.dq_acc + (static_cast<size_t>(bh) * a.N + row) * D);

@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(smem_u32(&bars->q_full[t]), 1);
       mbar_init(smem_u32(&bars->q_empty[t]), 1);
       mbar_init(smem_u32(&bars->s_full[t]), 1);
-      mbar_init(smem_u32(&bars->p_full[t]), 128);
+      mbar_init(smem_u32(&bars->p_full[t]), 4);  // one elected lane per softmax warp
       mbar_init(smem_u32(&bars->o_done[t]), 1);
     }
     for (int s = 0; s < Cfg::kStages; ++s) {
@@ -210,25 +210,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
 
       // S_t = Q_t K^T over d in steps of 16
+      // descriptors are built once per tile; a K step adds a constant
+      const SmemDesc dq[2] = {make_desc_sw128(sQ, 16, 1024),
+                              make_desc_sw128(sQ + Cfg::kTileBytes, 16, 1024)};
       auto issue_s = [&](int t, uint32_t slot) {
         const uint32_t dst = tmem + Cfg::col_s(t);
+        const SmemDesc da = dq[t];
+        const SmemDesc db = make_desc_sw128(sKV + slot * Cfg::kTileBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(sQ + t * Cfg::kTileBytes + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sKV + slot * Cfg::kTileBytes + off, 16, 1024);
-          mma_ss(dst, ad, bd, idesc_s, kk > 0);
+          mma_ss(dst, desc_at(da, off), desc_at(db, off), idesc_s, kk > 0);
         }
       };
       // O_t (+)= P_t V over the 128 keys in steps of 16
       auto issue_pv = [&](int t, uint32_t slot, bool accumulate) {
         const uint32_t dst = tmem + Cfg::col_o(t);
+        const uint32_t pa = tmem + Cfg::col_s(t);
+        const SmemDesc db = make_desc_sw128(sKV + slot * Cfg::kTileBytes, kBlockBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bd =
-              smem_desc_sw128(sKV + slot * Cfg::kTileBytes + kk * 2048, kBlockBytes, 1024);
-          mma_ts(dst, tmem + Cfg::col_s(t) + kk * 8, bd, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(dst, pa + kk * 8, desc_at(db, kk * 2048), idesc_o,
+                 (accumulate || kk > 0) ? 1u : 0u);
       };
 
       for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++q_round) {
@@ -396,7 +399,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars->p_full[t]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[t]));
         m = m_use;
         ++step;
       }

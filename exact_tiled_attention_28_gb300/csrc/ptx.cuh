@@ -184,6 +184,26 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same descriptor kept as its two 32-bit words. Stepping along K only
+// moves the start address, which sits in the low word and never carries out
+// of its 14 bits (shared memory is below 256 KiB), so the MMA-issuing thread
+// builds a tile's descriptor once and adds a constant per K step.
+struct SmemDesc {
+  uint32_t lo, hi;
+};
+
+__device__ __forceinline__ SmemDesc make_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+  SmemDesc d;
+  d.lo = ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+  d.hi = ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+  return d;
+}
+
+__device__ __forceinline__ uint64_t desc_at(SmemDesc d, uint32_t byte_offset) {
+  return (static_cast<uint64_t>(d.hi) << 32) | (d.lo + (byte_offset >> 4));
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32
 // accumulator. a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
