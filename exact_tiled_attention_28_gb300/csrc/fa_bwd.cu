@@ -44,7 +44,8 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 448;  // 8 compute warps, 4 dQ warps, load warp, MMA warp
+// four warpgroups: 0-1 compute, 2 dQ readout, 3 = load warp, MMA warp, two idle
+constexpr int kBwdThreads = 512;
 constexpr int kBwdDqWarp0 = 8;
 constexpr int kBwdLoadWarp = 12;
 constexpr int kBwdMmaWarp = 13;
@@ -196,8 +197,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// 448 threads: four warps on some SM sub-partitions, whose 16384-register
-// files then allow 128 registers per thread
+// 512 threads at 128 registers fill the register file (each SM sub-partition
+// holds one warp of every warpgroup: 4 x 32 x 128 = 16384). The warpgroups then
+// rebalance with setmaxnreg: compute 128, dQ readout 176, load/MMA 80; per
+// sub-partition 128 + 128 + 176 + 80 = 512 registers per lane, the launch total.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -254,6 +257,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  if (warp >= 12) {
+    setmaxnreg_dec<80>();
   if (warp == kBwdLoadWarp) {
     // ---------------------------------------------------------------- loader
     if (lane == 0) {
@@ -417,6 +422,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(smem_u32(&bars->drain));
       mbar_drain(smem_u32(&bars->drain), 0, 1000000000ull);
     }
+  }
   } else if (warp < 8) {
     // -------------------------------- compute warps: P^T and dS^T, 64 queries each
     const int wg = warp >> 2;            // query columns 64 wg .. 64 wg + 63
@@ -537,7 +543,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------- dQ warps: add dQ_i
-    if (warp >= kBwdDqWarp0 && warp < kBwdDqWarp0 + 4) {
+    setmaxnreg_inc<176>();
+    {
       const int wq = warp & 3;
       const uint32_t t_lane = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
       uint32_t it = 0;
@@ -552,24 +559,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
           if constexpr (D == 128) {
-            // lane = head-dim index dd, columns = the 128 queries of block i
-            // two halves of 64 queries (128 registers per thread at most); TMEM is
-            // released once the second half is in registers
+            // lane = head-dim index dd, columns = the 128 queries of block i.
+            // All 128 columns go to registers first and TMEM is released
+            // before any atomic is issued, so the next dP^T never waits on them.
             const int dd = wq * 32 + lane;
             const int rows = min(kTile, a.N - i * kTile);
             float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile) * D + dd;
-            uint32_t v[64];
+            uint32_t v[64], w[64];
             tmem_ld64(t_lane + kColDP, v);
-#pragma unroll
-            for (int q = 0; q < 64; ++q)
-              if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
-            tmem_ld64(t_lane + kColDP + 64, v);
+            tmem_ld64(t_lane + kColDP + 64, w);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
 #pragma unroll
             for (int q = 0; q < 64; ++q)
-              if (64 + q < rows) atomicAdd(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(v[q]));
+              if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
+#pragma unroll
+            for (int q = 0; q < 64; ++q)
+              if (64 + q < rows) atomicAdd(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(w[q]));
           } else {
             // lane = query row, columns = the d = 64 head-dim values
             uint32_t v[64];

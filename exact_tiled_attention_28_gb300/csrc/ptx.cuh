@@ -338,6 +338,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 #undef FA_W8
 
 // ---------------------------------------------------------------------------
+// per-warpgroup register budgets (all four warps of a warpgroup execute these)
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
 // arithmetic helpers
 
 __device__ __forceinline__ float ex2_approx(float x) {
