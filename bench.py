@@ -45,7 +45,9 @@ DEFAULT_WORKLOAD = "gpt_d128_n4096"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dK/dV kernel,
 # from an ncu capture of the current kernel source (see profiles/), keyed by
 # workload and causal flag; None where no capture of the current kernel exists.
-NCU_TRAFFIC_BYTES: dict = {}
+# Algorithmic bytes for comparison: q, k, v, dO read and dk, dv written once
+# (6 x 64 MiB) plus the fp32 dQ accumulator (128 MiB) = 537 MB at this size.
+NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.201e8}
 
 
 def fwd_flops(B, H, N, d, causal):
