@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     fa_bwd_workspace_size,
     fa_fwd,
     fa_last_device_status,
+    fa_selftest_exp2,
     fa_selftest_wait_timeout,
     fa_status_string,
     library_path,

@@ -23,7 +23,7 @@ FA_ERR_WORKSPACE = 5
 
 # every symbol include/fa.h declares
 EXPORTED = ("fa_abi_version", "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess",
-            "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout",
+            "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout", "fa_selftest_exp2",
             "fa_status_string", "fa_last_device_status")
 
 # fixed device scratch of fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in include/fa.h)
@@ -68,6 +68,8 @@ def load():
     lib.fa_bwd_dq_finalize.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_selftest_exp2.restype = i
+    lib.fa_selftest_exp2.argtypes = [vp, vp, i, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -159,6 +161,16 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 def fa_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
     _check(load().fa_selftest_wait_timeout(int(limit_ms), _stream_handle(stream)),
            "fa_selftest_wait_timeout")
+
+
+def fa_selftest_exp2(x, y, stream=None) -> None:
+    """y <- 2^x with the forward kernel's FMA-pipe exponential (CUDA fp32 tensors)."""
+    import torch
+    n = x.numel()
+    _dev_ptr(x, "x", torch.float32, x.shape)
+    _dev_ptr(y, "y", torch.float32, x.shape)
+    _check(load().fa_selftest_exp2(x.data_ptr(), y.data_ptr(), n, _stream_handle(stream)),
+           "fa_selftest_exp2")
 
 
 def fa_last_device_status(stream=None) -> int:

@@ -89,6 +89,18 @@ __global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
   mbar_wait(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
 }
 
+// Evaluates the forward kernel's FMA-pipe exp2 on n inputs.
+__global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i + 1 < n) {
+    const float2 r = exp2_poly2(make_float2(x[i], x[i + 1]));
+    y[i] = r.x;
+    y[i + 1] = r.y;
+  } else if (i < n) {
+    y[i] = exp2_poly2(make_float2(x[i], x[i])).x;
+  }
+}
+
 }  // namespace
 
 // Device facts for launchers outside this file (the no-alloc entry point).
@@ -207,6 +219,13 @@ fa_status fa_selftest_wait_timeout(int limit_ms, void* stream) {
   if (fa::device_info(&di) != cudaSuccess) return FA_ERR_CUDA;
   fa::wait_timeout_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
       di.status, static_cast<uint64_t>(limit_ms) * 1000000ull);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_selftest_exp2(const float* x, float* y, int n, void* stream) {
+  if (x == nullptr || y == nullptr || n < 1) return FA_ERR_INVALID_ARG;
+  const int threads = 256, blocks = (n / 2 + threads) / threads;
+  fa::exp2_selftest_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

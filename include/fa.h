@@ -146,6 +146,15 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
                          int H, int N, int d, int causal, float scale, void* stream);
 
+/*
+ * Self-test of the forward softmax's FMA-pipe exponential (no counterpart in
+ * the method; a numerical building block): y[i] = 2^x[i] for n >= 1 device
+ * floats, evaluated exactly as the forward kernel does for part of each row
+ * (range reduction, degree-3 polynomial, exponent insertion; inputs clamped
+ * at -125). Maximum relative error about 7.5e-5.
+ */
+fa_status fa_selftest_exp2(const float* x, float* y, int n, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(int status);
 

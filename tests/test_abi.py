@@ -118,3 +118,8 @@ def test_library_has_no_torch_dependency(lib):
     data = open(path, "rb").read()
     assert b"libtorch" not in data and b"libc10" not in data
     assert isinstance(lib, ctypes.CDLL)
+
+
+def test_exp2_selftest_rejects_before_launch(lib):
+    assert lib.fa_selftest_exp2(None, P, 4, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_selftest_exp2(P, P, 0, None) == fa.FA_ERR_INVALID_ARG
