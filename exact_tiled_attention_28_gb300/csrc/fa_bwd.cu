@@ -40,6 +40,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace fa {
 namespace {
@@ -266,7 +267,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t pol_q = policy_evict_last();
       uint32_t st_it = 0, kv_round = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
+        const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
+        if (item >= a.n_items) break;  // only in the last, partial round
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
         ok = mbar_wait(smem_u32(&bars->kv_empty), (kv_round & 1) ^ 1, abort, a.status);
@@ -360,7 +363,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       };
 
-      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++kv_round) {
+      for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd, ++kv_round) {
+        const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
+        if (item >= a.n_items) break;  // only in the last, partial round
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
         const int i0 = CAUSAL ? j : 0;
@@ -436,7 +441,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // row r of query block wg of dS^T in shared memory: 128-byte rows, 16-byte
     // chunks stored at chunk ^ (r & 7)
     const uint32_t ds_row = sDS + wg * kBlk + r * 128;
-    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++kv_round) {
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd, ++kv_round) {
+      const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
+      if (item >= a.n_items) break;  // only in the last, partial round
       int bh, j;
       decode_kv_item(item, a, CAUSAL, bh, j);
       const int i0 = CAUSAL ? j : 0;
@@ -549,7 +556,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t t_lane = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
       uint32_t it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
+        const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
+        if (item >= a.n_items) break;  // only in the last, partial round
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
         const int n_it = CAUSAL ? n_q - j : n_q;

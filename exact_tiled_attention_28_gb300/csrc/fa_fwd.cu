@@ -34,6 +34,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace fa {
 namespace {
@@ -163,7 +164,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t kv_it = 0;
       uint32_t q_issued[2] = {0u, 0u};
       bool ok = true;
-      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
+        const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
+        if (item >= a.n_items) break;  // only in the last, partial round
         int bh, pair;
         decode_item(item, a, CAUSAL, bh, pair);
         const int J = max(tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL));
@@ -244,7 +247,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                  (accumulate || kk > 0) ? 1u : 0u);
       };
 
-      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++q_round) {
+      for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd, ++q_round) {
+        const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
+        if (item >= a.n_items) break;  // only in the last, partial round
         int bh, pair;
         decode_item(item, a, CAUSAL, bh, pair);
         const int Jt[2] = {tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL)};
@@ -327,7 +332,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float NEG_INF = __int_as_float(0xff800000);
     uint32_t step = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
+      const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
+      if (item >= a.n_items) break;  // only in the last, partial round
       int bh, pair;
       decode_item(item, a, CAUSAL, bh, pair);
       const int qt = 2 * pair + t;
