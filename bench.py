@@ -40,6 +40,9 @@ WORKLOADS = {"b1_h2_n128_d64": (1, 2, 128, 64), "b4_h8_n1024_d64": (4, 8, 1024, 
 for _d, _H in ((64, 32), (128, 16)):
     for _N in (512, 1024, 2048, 4096, 8192, 16384):
         WORKLOADS[f"gpt_d{_d}_n{_N}"] = (16384 // _N, _H, _N, _d)
+# the other supported head dims, same token count (hidden 2048 at d = 32)
+WORKLOADS["dim_d32_n4096"] = (4, 64, 4096, 32)
+WORKLOADS["dim_d96_n4096"] = (4, 16, 4096, 96)
 DEFAULT_WORKLOAD = "gpt_d128_n4096"
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dK/dV kernel,

@@ -67,7 +67,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 fa_status check_sizes(int B, int H, int N, int d, float scale) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * H >= (int64_t(1) << 31)) return FA_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
@@ -138,7 +138,7 @@ const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null or misaligned pointer, size < 1 or bad scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension must be 64 or 128";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension must be 32, 64, 96 or 128";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side bounded wait expired";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: backward workspace null or too small";

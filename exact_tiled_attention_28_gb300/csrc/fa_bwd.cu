@@ -57,8 +57,9 @@ constexpr int kSmemSpare = 768;  // bytes left for aligning the dynamic base to 
 
 template <int D>
 struct BwdCfg {
-  static constexpr int kColBlocks = D / 64;
-  static constexpr int kTileBytes = kTile * D * 2;
+  // d = 32 and 96 use whole 64-column blocks (TMA zero-fills past d)
+  static constexpr int kColBlocks = (D + 63) / 64;
+  static constexpr int kTileBytes = kTile * kColBlocks * 64 * 2;
   static constexpr int kStages = 2;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;  // Q_i, dO_i, lse2 and D rows
   static constexpr int kOffK = 0;
@@ -83,6 +84,7 @@ constexpr int bwd_smem_bytes() {
 }
 static_assert(bwd_smem_bytes<128>() <= 232448, "backward shared memory over the sm_103a limit");
 static_assert(bwd_smem_bytes<64>() <= 232448, "backward shared memory over the sm_103a limit");
+static_assert(bwd_smem_bytes<96>() <= 232448, "backward shared memory over the sm_103a limit");
 
 struct BwdArgs {
   const __nv_bfloat16* o;
@@ -104,7 +106,10 @@ struct BwdArgs {
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
-  constexpr int kLanesPerRow = D / 8;  // each lane handles 8 elements (16 bytes)
+  // each active lane handles 8 elements (16 bytes) of a row; rows take a
+  // power-of-two number of lanes, the ones past d / 8 idle (d = 96)
+  constexpr int kLanesPerRow = D <= 32 ? 4 : (D <= 64 ? 8 : 16);
+  constexpr int kActive = D / 8;
   const size_t rows = static_cast<size_t>(a.BH) * a.Npad;
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     const int bh = static_cast<int>(row / a.Npad);
     const int i = static_cast<int>(row % a.Npad);
     float dot = 0.f;
-    if (i < a.N) {
+    if (i < a.N && part < kActive) {
       const size_t e = (static_cast<size_t>(bh) * a.N + i) * D + part * 8;
       const uint4 ov = *reinterpret_cast<const uint4*>(a.o + e);
       const uint4 gv = *reinterpret_cast<const uint4*>(a.dO + e);
@@ -587,9 +592,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int q = 0; q < 64; ++q)
               if (64 + q < rows) atomicAdd(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(w[q]));
           } else {
-            // lane = query row, columns = the d = 64 head-dim values
-            uint32_t v[64];
-            tmem_ld64(t_lane + kColDP, v);
+            // lane = query row, columns = the d head-dim values
+            uint32_t v[D];
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t t32[32];
+              tmem_ld32(t_lane + kColDP + c0, t32);
+#pragma unroll
+              for (int u = 0; u < 32; ++u) v[c0 + u] = t32[u];
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
@@ -618,7 +629,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const BwdArgs& a,
                          int stages, cudaStream_t stream) {
   if (stages & kStagePre) {
-    const size_t work = static_cast<size_t>(a.BH) * a.Npad * (D / 8);
+    const size_t work = static_cast<size_t>(a.BH) * a.Npad * (D <= 32 ? 4 : (D <= 64 ? 8 : 16));
     const int grid = static_cast<int>(std::min<size_t>((work + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
     bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(a);
     const cudaError_t e = cudaGetLastError();
@@ -679,11 +690,20 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
   a.status = p.status;
   a.scale = p.scale;
   a.scale_log2 = p.scale * 1.4426950408889634f;
-  if (p.d == 64)
-    return p.causal ? launch_bwd_t<64, true>(p, maps, a, stages, stream)
-                    : launch_bwd_t<64, false>(p, maps, a, stages, stream);
-  return p.causal ? launch_bwd_t<128, true>(p, maps, a, stages, stream)
-                  : launch_bwd_t<128, false>(p, maps, a, stages, stream);
+  switch (p.d) {
+    case 32:
+      return p.causal ? launch_bwd_t<32, true>(p, maps, a, stages, stream)
+                      : launch_bwd_t<32, false>(p, maps, a, stages, stream);
+    case 64:
+      return p.causal ? launch_bwd_t<64, true>(p, maps, a, stages, stream)
+                      : launch_bwd_t<64, false>(p, maps, a, stages, stream);
+    case 96:
+      return p.causal ? launch_bwd_t<96, true>(p, maps, a, stages, stream)
+                      : launch_bwd_t<96, false>(p, maps, a, stages, stream);
+    default:
+      return p.causal ? launch_bwd_t<128, true>(p, maps, a, stages, stream)
+                      : launch_bwd_t<128, false>(p, maps, a, stages, stream);
+  }
 }
 
 }  // namespace fa

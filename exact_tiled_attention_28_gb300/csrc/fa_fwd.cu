@@ -62,9 +62,12 @@ constexpr int kBlockBytes = kTile * 64 * 2;  // one 128-row x 64-column bf16 blo
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kColBlocks = D / 64;
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  // head dims that are not a multiple of 64 (32, 96) use whole 64-column
+  // blocks in shared memory; TMA zero-fills the columns past d and the MMAs
+  // only read the first d
+  static constexpr int kColBlocks = (D + 63) / 64;
+  static constexpr int kTileBytes = kTile * kColBlocks * 64 * 2;
+  static constexpr int kStages = (kColBlocks == 2) ? 4 : 8;
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kTileBytes;
   // TMEM column of S_t and of O_t
@@ -498,11 +501,20 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const voi
   a.n_items = BH * a.n_pairs;
   a.scale = p.scale;
   a.scale_log2 = p.scale * 1.4426950408889634f;
-  if (p.d == 64)
-    return p.causal ? launch_fwd_t<64, true>(p, mq, mk, mv, a, stream)
-                    : launch_fwd_t<64, false>(p, mq, mk, mv, a, stream);
-  return p.causal ? launch_fwd_t<128, true>(p, mq, mk, mv, a, stream)
-                  : launch_fwd_t<128, false>(p, mq, mk, mv, a, stream);
+  switch (p.d) {
+    case 32:
+      return p.causal ? launch_fwd_t<32, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<32, false>(p, mq, mk, mv, a, stream);
+    case 64:
+      return p.causal ? launch_fwd_t<64, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<64, false>(p, mq, mk, mv, a, stream);
+    case 96:
+      return p.causal ? launch_fwd_t<96, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<96, false>(p, mq, mk, mv, a, stream);
+    default:
+      return p.causal ? launch_fwd_t<128, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<128, false>(p, mq, mk, mv, a, stream);
+  }
 }
 
 }  // namespace fa

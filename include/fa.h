@@ -22,7 +22,7 @@
  *    contiguous, d innermost. lse is fp32 [B, H, N] (natural log).
  *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
  *    aligned. The library keeps no reference to them after the call.
- *  - d must be 64 or 128; B, H, N >= 1; B*H < 2^31 (offsets are computed in
+ *  - d must be 32, 64, 96 or 128; B, H, N >= 1; B*H < 2^31 (offsets are computed in
  *    64 bits, so a tensor may hold more than 2^31 elements).
  *  - Causal masking is top-left aligned with equal query and key lengths:
  *    query i sees keys j <= i. scale must be finite and >= 0.
@@ -47,7 +47,7 @@ extern "C" {
 typedef enum fa_status {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, size < 1, bad scale */
-  FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 or 128, too large */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension not 32/64/96/128, or B*H too large */
   FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FA_ERR_TIMEOUT = 4,     /* a device-side bounded wait expired */
   FA_ERR_WORKSPACE = 5    /* backward workspace null or too small */

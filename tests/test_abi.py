@@ -75,7 +75,8 @@ def bwd(lib, ws=P, ws_bytes=None, B=1, H=1, N=128, d=64, scale=0.125, null=None)
     (dict(B=0), fa.FA_ERR_INVALID_ARG),
     (dict(H=-1), fa.FA_ERR_INVALID_ARG),
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
-    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=80), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=48), fa.FA_ERR_UNSUPPORTED),
     (dict(d=256), fa.FA_ERR_UNSUPPORTED),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
@@ -89,14 +90,15 @@ def test_fwd_rejects_before_launch(lib, kw, want):
 def test_bwd_rejects_before_launch(lib):
     for i in range(9):
         assert bwd(lib, null=i) == fa.FA_ERR_INVALID_ARG
-    assert bwd(lib, d=32) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(lib, d=48) == fa.FA_ERR_UNSUPPORTED
     assert bwd(lib, ws=None) == fa.FA_ERR_WORKSPACE
     assert bwd(lib, ws=P + 4) == fa.FA_ERR_WORKSPACE
     assert bwd(lib, ws_bytes=fa.fa_bwd_workspace_size(1, 1, 128, 64) - 1) == fa.FA_ERR_WORKSPACE
 
 
 def test_workspace_size(lib):
-    for B, H, N, d in ((1, 1, 1, 64), (4, 8, 1024, 64), (1, 16, 32768, 128), (2, 3, 77, 128)):
+    for B, H, N, d in ((1, 1, 1, 64), (4, 8, 1024, 64), (1, 16, 32768, 128), (2, 3, 77, 128),
+                       (2, 2, 100, 32), (1, 3, 300, 96)):
         assert fa.fa_bwd_workspace_size(B, H, N, d) >= 4 * B * H * N * (d + 1)
     assert fa.fa_bwd_workspace_size(1, 1, 0, 64) == 0
     assert fa.fa_bwd_workspace_size(1, 1, 16, 80) == 0

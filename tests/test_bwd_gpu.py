@@ -35,14 +35,14 @@ def test_config_b4_h8_n1024_d64(cuda_lib, causal):
     _full_check(cuda_lib, 2, 4, 8, 1024, 64, causal)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 2, 77, 128, 129, 200, 383, 640])
 def test_ragged_lengths(cuda_lib, N, d, causal):
     _full_check(cuda_lib, 100 + N, 2, 3, N, d, causal)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_many_heads_spread_over_persistent_ctas(cuda_lib, d, causal):
     _full_check(cuda_lib, 8, 3, 40, 384, d, causal)
