@@ -20,8 +20,8 @@
 //       P^T, dS^T by two compute warpgroups, one thread per key row, each
 //       warpgroup owning 64 of the 128 query columns  (TMEM <-> regs)
 //       dV += P^T dO_i and dK += dS^T Q_i           (tcgen05, A from TMEM)
-//       d = 128: dQ_i^T = K_j^T dS^T                (tcgen05, both from SMEM)
-//       d = 64:  dQ_i = dS K_j                      (tcgen05, both from SMEM)
+//       d >= 64: dQ_i^T = K_j^T dS^T (M = 128)      (tcgen05, both from SMEM)
+//       d = 32:  dQ_i = dS K_j                      (tcgen05, both from SMEM)
 //     and four more warps read dQ_i out of TMEM and add it to the fp32
 //     accumulator in global memory. With dQ^T in TMEM (lanes = head dim,
 //     columns = queries) a warp's 32 atomics cover one contiguous 128-byte
@@ -67,6 +67,13 @@ struct BwdCfg {
   static constexpr int kOffDS = 2 * kTileBytes;             // dS^T, 128 x 128 bf16
   static constexpr int kOffStages = 2 * kTileBytes + kTile * kTile * 2;
   static constexpr int kOffBars = kOffStages + kStages * kStageBytes;
+  // d >= 64: dQ_i^T = K^T dS^T with M = 128, read out with coalesced atomics.
+  // The MMA's rows past d are never stored: at d = 96 they read the K tile's
+  // zero-filled columns, at d = 64 the V tile that follows K in shared memory
+  // (finite values, results discarded). Measured on GB300 at d = 64 this
+  // still beats dQ_i = dS K with one scattered row per thread by 22%.
+  // d = 32: dQ_i = dS K with one row per thread.
+  static constexpr bool kDqTransposed = D >= 64;
   static constexpr uint32_t col_dk() { return kColDV + D; }
 };
 
@@ -331,7 +338,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_acc = idesc_bf16_f32(kTile, D, false, true);
       // d = 128: dQ^T = K^T dS^T (M = d, N = 128 queries); d = 64: dQ = dS K
       // (M = 128 queries, N = d). Both operands MN-major in SMEM.
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(kTile, D == 128 ? kTile : D, true, true);
+      constexpr uint32_t idesc_dq =
+          idesc_bf16_f32(kTile, Cfg::kDqTransposed ? kTile : D, true, true);
       uint32_t st_it = 0, kv_round = 0, it = 0;
       bool ok = true;
 
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t ds_desc = desc_at(d_ds, kk * 2048);
           const uint64_t k_desc = desc_at(d_kmn, kk * 2048);
-          if constexpr (D == 128)
+          if constexpr (Cfg::kDqTransposed)
             mma_ss(tmem + kColDP, k_desc, ds_desc, idesc_dq, kk > 0);
           else
             mma_ss(tmem + kColDP, ds_desc, k_desc, idesc_dq, kk > 0);
@@ -572,7 +580,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = mbar_wait_warp(smem_u32(&bars->dq_full), it & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
-          if constexpr (D == 128) {
+          if constexpr (Cfg::kDqTransposed) {
             // lane = head-dim index dd, columns = the 128 queries of block i.
             // All 128 columns go to registers first and TMEM is released
             // before any atomic is issued, so the next dP^T never waits on them.
@@ -585,12 +593,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+            if (wq * 32 < D) {  // whole warps of head-dim rows past d hold zeros
 #pragma unroll
-            for (int q = 0; q < 64; ++q)
-              if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
+              for (int q = 0; q < 64; ++q)
+                if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
 #pragma unroll
-            for (int q = 0; q < 64; ++q)
-              if (64 + q < rows) atomicAdd(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(w[q]));
+              for (int q = 0; q < 64; ++q)
+                if (64 + q < rows)
+                  atomicAdd(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(w[q]));
+            }
           } else {
             // lane = query row, columns = the d head-dim values
             uint32_t v[D];
