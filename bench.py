@@ -50,7 +50,7 @@ DEFAULT_WORKLOAD = "gpt_d128_n4096"
 # workload and causal flag; None where no capture of the current kernel exists.
 # Algorithmic bytes for comparison: q, k, v, dO read and dk, dv written once
 # (6 x 64 MiB) plus the fp32 dQ accumulator (128 MiB) = 537 MB at this size.
-NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.201e8}
+NCU_TRAFFIC_BYTES: dict = {}
 
 
 def fwd_flops(B, H, N, d, causal):
@@ -159,6 +159,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--layout", default="bhnd", choices=("bhnd", "bnhd"),
+                    help="memory layout of q, k, v, o, dO and the gradients")
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
@@ -178,7 +180,7 @@ def config_of(args, B, H, N, d):
                         f"{'causal' if args.causal else 'non-causal'} fwd+bwd",
             "B": B, "H": H, "N": N, "d": d, "causal": bool(args.causal),
             "scale": "1/sqrt(d)", "global_batch": B * args.gpus, "seq_len": N,
-            "parallelism": f"replicas x{args.gpus}",
+            "parallelism": f"replicas x{args.gpus}", "layout": args.layout,
             "l2": "inputs larger than L2" if 8 * B * H * N * d * 2 > 129e6 else "L2-resident"}
 
 
@@ -218,7 +220,7 @@ def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, st
     bufs = [({n: t for n, t in x0.items()}, outs0, ws0),
             ({n: torch.empty_like(t) for n, t in x0.items()},
              {n: torch.empty_like(t) for n, t in outs0.items()}, torch.empty_like(ws0))]
-    out_host = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs0.items()}
+    out_host = [{n: torch.empty_like(t, device="cpu").pin_memory() for n, t in outs0.items()}
                 for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs0.values())
@@ -292,10 +294,18 @@ def run_ours(args):
 
     bits = inputs.attention_inputs(seed, B, H, N, d)
     host = {n: inputs.bits_to_torch_bf16(b).pin_memory() for n, b in bits.items()}
-    x = {n: t.to(dev) for n, t in host.items()}
-    o = torch.empty_like(x["q"])
+    if args.layout == "bnhd":
+        # [B, N, H, d] storage, passed as [B, H, N, d] views (strided entry points)
+        host = {n: t.transpose(1, 2).contiguous().pin_memory().transpose(1, 2)
+                for n, t in host.items()}
+        x = {n: t.transpose(1, 2).to(dev).transpose(1, 2) for n, t in host.items()}
+        new = lambda: torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev).transpose(1, 2)
+    else:
+        x = {n: t.to(dev) for n, t in host.items()}
+        new = lambda: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    o = new()
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    dq, dk, dv = new(), new(), new()
     ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -305,8 +315,17 @@ def run_ours(args):
         fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, causal, scale)
         if ev is not None:
             ev[1].record(stream)
-        fa.fa_bwd_stages(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, causal, scale, ws,
-                         events=None if ev is None else ev[2:6])
+        if args.layout == "bhnd":
+            fa.fa_bwd_stages(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, causal, scale,
+                             ws, events=None if ev is None else ev[2:6])
+        else:  # the staged entry points take contiguous tensors: time fa_bwd as a whole
+            if ev is not None:
+                ev[2].record(stream)
+                ev[3].record(stream)
+            fa.fa_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, causal, scale, ws)
+            if ev is not None:
+                ev[4].record(stream)
+                ev[5].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -359,7 +378,7 @@ def run_ours(args):
     value = replicas.aggregate_throughput(3.5 * F, world, ms_step_max)
     dkdv_tf = 2.5 * F / (dkdv_ms * 1e-3) / 1e12
     fwd_tf = F / (fwd_ms * 1e-3) / 1e12
-    traffic = NCU_TRAFFIC_BYTES.get((args.workload, causal))
+    traffic = NCU_TRAFFIC_BYTES.get((args.workload, causal)) if args.layout == "bhnd" else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -375,7 +394,8 @@ def run_ours(args):
                     "frac_of_sustained_peak": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peaks["sustained"]},
         "bwd": {"ms": bwd_ms, "pre_ms": pre_ms, "dkdv_ms": dkdv_ms, "dq_ms": dq_ms,
                 "tflops": 2.5 * F / (bwd_ms * 1e-3) / 1e12},
-        "roofline": {"kernel": "bwd_dkdv_kernel", "bound": "tensor", "achieved": dkdv_tf,
+        "roofline": {"kernel": "bwd_dkdv_kernel" if args.layout == "bhnd" else "fa_bwd (all stages)",
+                     "bound": "tensor", "achieved": dkdv_tf,
                      "peak": peaks["sustained"], "unit": "TFLOP/s",
                      "frac": dkdv_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}",
                      "traffic": traffic,

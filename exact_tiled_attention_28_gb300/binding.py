@@ -22,7 +22,8 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
 
 # every symbol include/fa.h declares
-EXPORTED = ("fa_abi_version", "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess",
+EXPORTED = ("fa_abi_version", "fa_fwd", "fa_fwd_strided", "fa_bwd_workspace_size", "fa_bwd",
+            "fa_bwd_strided", "fa_bwd_preprocess",
             "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout", "fa_selftest_exp2",
             "fa_status_string", "fa_last_device_status")
 
@@ -56,6 +57,12 @@ def load():
     lib.fa_abi_version.argtypes = []
     lib.fa_fwd.restype = i
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    ll = ctypes.POINTER(ctypes.c_longlong)
+    lib.fa_fwd_strided.restype = i
+    lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ll, i, f, vp]
+    lib.fa_bwd_strided.restype = i
+    lib.fa_bwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, ll, i, f, vp,
+                                   sz, vp]
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
@@ -108,16 +115,33 @@ def _shape(q):
     return tuple(int(x) for x in q.shape)
 
 
-def _dev_ptr(t, name, dtype, shape):
-    import torch
+def _dev_ptr(t, name, dtype, shape, strided=False):
+    """Device pointer of a tensor. With strided=True any view of that shape
+    whose last dimension is contiguous is accepted; otherwise the tensor must
+    be contiguous."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}")
-    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous with shape {tuple(shape)}")
-    del torch
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}")
+    if strided:
+        if t.stride(-1) != 1 and t.shape[-1] > 1:
+            raise ValueError(f"{name}: the last dimension must be contiguous")
+    elif not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
+
+
+def _strides(tensors):
+    """ctypes array of (batch, head, row) element strides of [B, H, N, d] views,
+    or None when every view is contiguous."""
+    if all(t.is_contiguous() for t in tensors):
+        return None
+    vals = []
+    for t in tensors:
+        vals += [int(t.stride(0)), int(t.stride(1)), int(t.stride(2))]
+    return (ctypes.c_longlong * len(vals))(*vals)
 
 
 # ---------------------------------------------------------------------------
@@ -181,13 +205,23 @@ def fa_last_device_status(stream=None) -> int:
 # tensor-level calls
 
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
-    """o, lse <- attention(q, k, v) on the current (or given) CUDA stream."""
+    """o, lse <- attention(q, k, v) on the current (or given) CUDA stream.
+
+    q, k, v, o are [B, H, N, d] bf16 views with a contiguous last dimension (a
+    [B, N, H, d] tensor passed as .transpose(1, 2), or K and V slices of one
+    packed buffer, go through fa_fwd_strided); lse is contiguous fp32 [B, H, N]."""
     import torch
     B, H, N, d = _shape(q)
     bf = torch.bfloat16
-    args = [_dev_ptr(t, n, bf, (B, H, N, d)) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
+    ts = ((q, "q"), (k, "k"), (v, "v"), (o, "o"))
+    args = [_dev_ptr(t, n, bf, (B, H, N, d), strided=True) for t, n in ts]
     args.append(_dev_ptr(lse, "lse", torch.float32, (B, H, N)))
-    _check(fa_fwd_raw(*args, B, H, N, d, causal, scale, _stream_handle(stream)), "fa_fwd")
+    st = _strides([t for t, _ in ts])
+    if st is None:
+        _check(fa_fwd_raw(*args, B, H, N, d, causal, scale, _stream_handle(stream)), "fa_fwd")
+    else:
+        _check(load().fa_fwd_strided(*args, B, H, N, d, st, int(bool(causal)), float(scale),
+                                     _stream_handle(stream)), "fa_fwd_strided")
 
 
 def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace,
@@ -197,15 +231,20 @@ def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspac
     import torch
     B, H, N, d = _shape(q)
     bf = torch.bfloat16
-    ptrs = [_dev_ptr(t, n, bf, (B, H, N, d))
-            for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
-    ptrs.append(_dev_ptr(lse, "lse", torch.float32, (B, H, N)))
-    ptrs += [_dev_ptr(t, n, bf, (B, H, N, d))
-             for t, n in ((do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))]
+    ts = ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))
+    p = {n: _dev_ptr(t, n, bf, (B, H, N, d), strided=True) for t, n in ts}
+    pl = _dev_ptr(lse, "lse", torch.float32, (B, H, N))
     if not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
-    _check(fa_bwd_raw(*ptrs, B, H, N, d, causal, scale, workspace.data_ptr(),
-                      workspace.numel(), _stream_handle(stream)), "fa_bwd")
+    ptrs = [p["q"], p["k"], p["v"], p["o"], pl, p["do"], p["dq"], p["dk"], p["dv"]]
+    st = _strides([t for t, _ in ts])
+    if st is None:
+        _check(fa_bwd_raw(*ptrs, B, H, N, d, causal, scale, workspace.data_ptr(),
+                          workspace.numel(), _stream_handle(stream)), "fa_bwd")
+    else:
+        _check(load().fa_bwd_strided(*ptrs, B, H, N, d, st, int(bool(causal)), float(scale),
+                                     workspace.data_ptr(), workspace.numel(),
+                                     _stream_handle(stream)), "fa_bwd_strided")
 
 
 def fa_bwd_stages(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace,

@@ -72,6 +72,16 @@ fa_status check_sizes(int B, int H, int N, int d, float scale) {
   return FA_OK;
 }
 
+// Strides (in elements) of a [B, H, N, d] tensor whose rows hold d
+// contiguous values: positive multiples of 8 (16 bytes, for TMA and 16-byte
+// stores), rows at least d apart, below 2^36 elements.
+fa_status check_strides(const long long* st, int n) {
+  if (st == nullptr) return FA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3 * n; ++i)
+    if (st[i] <= 0 || (st[i] & 7) != 0 || st[i] >= (1ll << 36)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
 fa_status check_ptrs(std::initializer_list<const void*> ptrs) {
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID_ARG;
@@ -113,15 +123,17 @@ cudaError_t current_device_setup(int* num_sms, int** status) {
   return cudaSuccess;
 }
 
-bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
+                   const Strides& s) {
   if (!g_encode) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(N) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.row) * 2,
+                                 static_cast<cuuint64_t>(s.head) * 2,
+                                 static_cast<cuuint64_t>(s.batch) * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTile), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -146,17 +158,44 @@ const char* fa_status_string(int status) {
   }
 }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                 int N, int d, int causal, float scale, void* stream) {
+namespace {
+
+// strides: 3 per tensor (batch, head, row) in TensorId order, or null for
+// contiguous [B, H, N, d] tensors
+fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, const long long* strides, int causal, float scale,
+                     void* stream) {
   fa_status s = fa::check_sizes(B, H, N, d, scale);
   if (s != FA_OK) return s;
   s = fa::check_ptrs({q, k, v, o, lse});
   if (s != FA_OK) return s;
+  if (strides != nullptr) {
+    s = fa::check_strides(strides, 4);
+    if (s != FA_OK) return s;
+  }
   fa::DeviceInfo di;
   if (fa::device_info(&di) != cudaSuccess) return FA_ERR_CUDA;
-  fa::Problem p{B, H, N, d, causal ? 1 : 0, scale, di.num_sms, di.status};
+  fa::Problem p{B, H, N, d, causal ? 1 : 0, scale, di.num_sms, di.status, {}};
+  for (int t = 0; t < fa::kNumTensors; ++t)
+    p.st[t] = (strides != nullptr && t < 4)
+                  ? fa::Strides{strides[3 * t], strides[3 * t + 1], strides[3 * t + 2]}
+                  : fa::contiguous_strides(H, N, d);
   const cudaError_t e = fa::launch_fwd(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, N, d, nullptr, causal, scale, stream);
+}
+
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, const long long* strides, int causal, float scale,
+                         void* stream) {
+  if (strides == nullptr) return FA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, H, N, d, strides, causal, scale, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -169,17 +208,25 @@ namespace {
 fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                      int causal, float scale, void* workspace, size_t workspace_bytes, int stages,
-                     std::initializer_list<const void*> used, void* stream) {
+                     std::initializer_list<const void*> used, void* stream,
+                     const long long* strides = nullptr) {
   fa_status s = fa::check_sizes(B, H, N, d, scale);
   if (s != FA_OK) return s;
   s = fa::check_ptrs(used);
   if (s != FA_OK) return s;
+  if (strides != nullptr) {
+    s = fa::check_strides(strides, fa::kNumTensors);
+    if (s != FA_OK) return s;
+  }
   if (workspace == nullptr || !fa::aligned16(workspace) ||
       workspace_bytes < fa::bwd_workspace_bytes(B, H, N, d))
     return FA_ERR_WORKSPACE;
   fa::DeviceInfo di;
   if (fa::device_info(&di) != cudaSuccess) return FA_ERR_CUDA;
-  fa::Problem p{B, H, N, d, causal ? 1 : 0, scale, di.num_sms, di.status};
+  fa::Problem p{B, H, N, d, causal ? 1 : 0, scale, di.num_sms, di.status, {}};
+  for (int t = 0; t < fa::kNumTensors; ++t)
+    p.st[t] = strides != nullptr ? fa::Strides{strides[3 * t], strides[3 * t + 1], strides[3 * t + 2]}
+                                 : fa::contiguous_strides(H, N, d);
   const cudaError_t e = fa::launch_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, workspace, stages,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -192,6 +239,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, workspace,
                     workspace_bytes, fa::kStagesAll, {q, k, v, o, lse, dO, dq, dk, dv}, stream);
+}
+
+fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, const long long* strides, int causal, float scale,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (strides == nullptr) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+                    workspace_bytes, fa::kStagesAll, {q, k, v, o, lse, dO, dq, dk, dv}, stream,
+                    strides);
 }
 
 fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dO, int B, int H, int N,

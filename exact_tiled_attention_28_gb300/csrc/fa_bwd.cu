@@ -93,31 +93,68 @@ static_assert(bwd_smem_bytes<128>() <= 232448, "backward shared memory over the 
 static_assert(bwd_smem_bytes<64>() <= 232448, "backward shared memory over the sm_103a limit");
 static_assert(bwd_smem_bytes<96>() <= 232448, "backward shared memory over the sm_103a limit");
 
-struct BwdArgs {
+// The workspace: D and the lse rows in log2 units, each fp32 [BH, Npad], then
+// the fp32 dQ accumulator [BH, N, d].
+struct Workspace {
+  float* base;
+  __device__ __forceinline__ float* Drow(int BH, int Npad) const { return base; }
+  __device__ __forceinline__ float* lse2(int BH, int Npad) const {
+    return base + static_cast<size_t>(BH) * Npad;
+  }
+  __device__ __forceinline__ float* dq_acc(int BH, int Npad) const {
+    return base + 2 * static_cast<size_t>(BH) * Npad;
+  }
+};
+
+// Each kernel gets only the arguments it reads. The dK/dV kernel's struct is
+// kept at 112 bytes: with more (even unused) bytes appended, its launches ran
+// 3-12% slower on GB300 with this compiler.
+struct PreArgs {
   const __nv_bfloat16* o;
   const __nv_bfloat16* dO;
   const float* lse;
-  float* Drow;    // [BH, Npad]
-  float* lse2;    // [BH, Npad]
-  float* dq_acc;  // [BH, N, d]
+  Workspace ws;
+  Strides so, sdo;  // element strides of o and dO
+  int N, H, Npad, BH;
+};
+
+struct DqArgs {
+  Workspace ws;
   __nv_bfloat16* dq;
+  Strides sdq;
+  int N, H, Npad, BH;
+  float scale;
+};
+
+struct BwdArgs {
+  Workspace ws;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int* status;
-  int N, Npad, BH, n_tiles, n_items;
+  int N, H, Npad, BH, n_tiles, n_items;
   float scale, scale_log2;
+  Strides sdk, sdv;  // element strides of dk and dv
 };
+static_assert(sizeof(BwdArgs) == 112, "dK/dV argument struct grew");
+
+// Element offset of row `row` of head bh (= b * H + h) in a strided tensor.
+__device__ __forceinline__ int64_t row_offset(const Strides& st, int bh, int H, int row) {
+  return (bh / H) * st.batch + (bh % H) * st.head + static_cast<int64_t>(row) * st.row;
+}
 
 // ---------------------------------------------------------------------------
 // 1. pre-pass
 
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
   // each active lane handles 8 elements (16 bytes) of a row; rows take a
   // power-of-two number of lanes, the ones past d / 8 idle (d = 96)
   constexpr int kLanesPerRow = D <= 32 ? 4 : (D <= 64 ? 8 : 16);
   constexpr int kActive = D / 8;
   const size_t rows = static_cast<size_t>(a.BH) * a.Npad;
+  float* const Drow = a.ws.Drow(a.BH, a.Npad);
+  float* const lse2 = a.ws.lse2(a.BH, a.Npad);
+  float* const dq_acc = a.ws.dq_acc(a.BH, a.Npad);
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
        g < rows * kLanesPerRow; g += nthreads) {
@@ -127,9 +164,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     const int i = static_cast<int>(row % a.Npad);
     float dot = 0.f;
     if (i < a.N && part < kActive) {
-      const size_t e = (static_cast<size_t>(bh) * a.N + i) * D + part * 8;
-      const uint4 ov = *reinterpret_cast<const uint4*>(a.o + e);
-      const uint4 gv = *reinterpret_cast<const uint4*>(a.dO + e);
+      const size_t e = (static_cast<size_t>(bh) * a.N + i) * D + part * 8;  // accumulator
+      const uint4 ov = *reinterpret_cast<const uint4*>(a.o + row_offset(a.so, bh, a.H, i) + part * 8);
+      const uint4 gv =
+          *reinterpret_cast<const uint4*>(a.dO + row_offset(a.sdo, bh, a.H, i) + part * 8);
       const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
       const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
@@ -139,7 +177,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
         dot = fmaf(of.x, gf.x, dot);
         dot = fmaf(of.y, gf.y, dot);
       }
-      float4* z = reinterpret_cast<float4*>(a.dq_acc + e);
+      float4* z = reinterpret_cast<float4*>(dq_acc + e);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -148,8 +186,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
       dot += __shfl_xor_sync(0xffffffffu, dot, off);
     if (part == 0) {
-      a.Drow[row] = dot;
-      a.lse2[row] = (i < a.N) ? a.lse[static_cast<size_t>(bh) * a.N + i] * 1.4426950408889634f
+      Drow[row] = dot;
+      lse2[row] = (i < a.N) ? a.lse[static_cast<size_t>(bh) * a.N + i] * 1.4426950408889634f
                               : __int_as_float(0x7f800000);
     }
   }
@@ -158,18 +196,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 // ---------------------------------------------------------------------------
 // 3. dq = bf16(scale * accumulator)
 
-__global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a, size_t n8) {
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const DqArgs a, size_t n8) {
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n8;
        g += nthreads) {
-    const float4* src = reinterpret_cast<const float4*>(a.dq_acc) + 2 * g;
+    const float4* src = reinterpret_cast<const float4*>(a.ws.dq_acc(a.BH, a.Npad)) + 2 * g;
     const float4 x = src[0], y = src[1];
+    const size_t row = g / (D / 8);  // accumulator row (b*H + h) * N + i
+    const int col = static_cast<int>(g % (D / 8)) * 8;
+    const int bh = static_cast<int>(row / a.N), i = static_cast<int>(row % a.N);
     uint4 w;
     w.x = pack_bf16x2(x.x * a.scale, x.y * a.scale);
     w.y = pack_bf16x2(x.z * a.scale, x.w * a.scale);
     w.z = pack_bf16x2(y.x * a.scale, y.y * a.scale);
     w.w = pack_bf16x2(y.z * a.scale, y.w * a.scale);
-    reinterpret_cast<uint4*>(a.dq)[g] = w;
+    *reinterpret_cast<uint4*>(a.dq + row_offset(a.sdq, bh, a.H, i) + col) = w;
   }
 }
 
@@ -270,7 +312,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp >= 12) {
+  if (warp >= kBwdLoadWarp) {
     setmaxnreg_dec<80>();
   if (warp == kBwdLoadWarp) {
     // ---------------------------------------------------------------- loader
@@ -284,14 +326,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (item >= a.n_items) break;  // only in the last, partial round
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
+        const int hh = bh % a.H, bb = bh / a.H;
         ok = mbar_wait(smem_u32(&bars->kv_empty), (kv_round & 1) ^ 1, abort, a.status);
         if (!ok) break;
         {
           const uint32_t bar = smem_u32(&bars->kv_full);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           for (int cb = 0; cb < Cfg::kColBlocks; ++cb) {
-            tma_load_3d(sK + cb * kBlk, &tmK, bar, 64 * cb, j * kTile, bh, pol_kv);
-            tma_load_3d(sV + cb * kBlk, &tmV, bar, 64 * cb, j * kTile, bh, pol_kv);
+            tma_load_4d(sK + cb * kBlk, &tmK, bar, 64 * cb, j * kTile, hh, bb, pol_kv);
+            tma_load_4d(sV + cb * kBlk, &tmV, bar, 64 * cb, j * kTile, hh, bb, pol_kv);
           }
           ++kv_round;
         }
@@ -306,13 +349,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t st = sSt + s * Cfg::kStageBytes;
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes + 1024);
           for (int cb = 0; cb < Cfg::kColBlocks; ++cb) {
-            tma_load_3d(st + cb * kBlk, &tmQ, bar, 64 * cb, i * kTile, bh, pol_q);
-            tma_load_3d(st + Cfg::kTileBytes + cb * kBlk, &tmdO, bar, 64 * cb, i * kTile, bh,
+            tma_load_4d(st + cb * kBlk, &tmQ, bar, 64 * cb, i * kTile, hh, bb, pol_q);
+            tma_load_4d(st + Cfg::kTileBytes + cb * kBlk, &tmdO, bar, 64 * cb, i * kTile, hh, bb,
                         pol_q);
           }
           const size_t roff = static_cast<size_t>(bh) * a.Npad + static_cast<size_t>(i) * kTile;
-          cp_bulk_g2s(st + 2 * Cfg::kTileBytes, a.lse2 + roff, 512, bar);
-          cp_bulk_g2s(st + 2 * Cfg::kTileBytes + 512, a.Drow + roff, 512, bar);
+          cp_bulk_g2s(st + 2 * Cfg::kTileBytes, a.ws.lse2(a.BH, a.Npad) + roff, 512, bar);
+          cp_bulk_g2s(st + 2 * Cfg::kTileBytes + 512, a.ws.Drow(a.BH, a.Npad) + roff, 512, bar);
           ++st_it;
         }
       }
@@ -343,10 +386,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t st_it = 0, kv_round = 0, it = 0;
       bool ok = true;
 
-      // descriptors are built once per tile; a K step adds a constant
+      // Descriptors are rebuilt at every issue from an opaque base (one add per
+      // K step): hoisted out of the loops they would not fit in the 80
+      // registers of this warpgroup and would spill.
       auto issue_kq = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile) {
-        const SmemDesc da = make_desc_sw128(a_tile, 16, 1024);
-        const SmemDesc db = make_desc_sw128(b_tile, 16, 1024);
+        const SmemDesc da = make_desc_sw128(opaque_u32(a_tile), 16, 1024);
+        const SmemDesc db = make_desc_sw128(opaque_u32(b_tile), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
@@ -356,15 +401,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // A = packed P^T or dS^T: queries 16kk..16kk+15 sit in the half of the
       // region written by compute warpgroup kk / 4, at column 64 (kk/4) + 8 (kk%4)
       auto issue_acc = [&](uint32_t dst, uint32_t a_region, uint32_t b_tile, bool accumulate) {
-        const SmemDesc db = make_desc_sw128(b_tile, kBlk, 1024);
+        const SmemDesc db = make_desc_sw128(opaque_u32(b_tile), kBlk, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(dst, a_region + 64 * (kk >> 2) + 8 * (kk & 3), desc_at(db, kk * 2048), idesc_acc,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
-      const SmemDesc d_ds = make_desc_sw128(sDS, kBlk, 1024);
-      const SmemDesc d_kmn = make_desc_sw128(sK, kBlk, 1024);
       auto issue_dq = [&]() {
+        const SmemDesc d_ds = make_desc_sw128(opaque_u32(sDS), kBlk, 1024);
+        const SmemDesc d_kmn = make_desc_sw128(opaque_u32(sK), kBlk, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t ds_desc = desc_at(d_ds, kk * 2048);
@@ -441,7 +486,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_drain(smem_u32(&bars->drain), 0, 1000000000ull);
     }
   }
-  } else if (warp < 8) {
+  } else if (warp < kBwdDqWarp0) {
     // -------------------------------- compute warps: P^T and dS^T, 64 queries each
     const int wg = warp >> 2;            // query columns 64 wg .. 64 wg + 63
     const int r = (warp & 3) * 32 + lane;  // key row within the block = TMEM lane
@@ -537,8 +582,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int key = j * kTile + r;
       const bool store = key < a.N;
-      const size_t base = (static_cast<size_t>(bh) * a.N + key) * D;
-      __nv_bfloat16* out = (wg == 0 ? a.dv : a.dk) + base;
+      __nv_bfloat16* out = wg == 0 ? a.dv + row_offset(a.sdv, bh, a.H, key)
+                                   : a.dk + row_offset(a.sdk, bh, a.H, key);
       const float mul = wg == 0 ? 1.f : a.scale;
       const uint32_t col = wg == 0 ? kColDV : Cfg::col_dk();
 #pragma unroll 1
@@ -586,7 +631,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // before any atomic is issued, so the next dP^T never waits on them.
             const int dd = wq * 32 + lane;
             const int rows = min(kTile, a.N - i * kTile);
-            float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile) * D + dd;
+            float* dst = a.ws.dq_acc(a.BH, a.Npad) + (static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile) * D + dd;
             uint32_t v[64], w[64];
             tmem_ld64(t_lane + kColDP, v);
             tmem_ld64(t_lane + kColDP + 64, w);
@@ -617,7 +662,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
             const int row = i * kTile + wq * 32 + lane;
             if (row < a.N) {
-              float4* dst = reinterpret_cast<float4*>(a.dq_acc + (static_cast<size_t>(bh) * a.N + row) * D);
+              float4* dst = reinterpret_cast<float4*>(a.ws.dq_acc(a.BH, a.Npad) + (static_cast<size_t>(bh) * a.N + row) * D);
 #pragma unroll
               for (int c = 0; c < D / 4; ++c)
                 atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
@@ -637,12 +682,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const BwdArgs& a,
-                         int stages, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const PreArgs& pa,
+                         const BwdArgs& a, const DqArgs& qa, int stages, cudaStream_t stream) {
   if (stages & kStagePre) {
     const size_t work = static_cast<size_t>(a.BH) * a.Npad * (D <= 32 ? 4 : (D <= 64 ? 8 : 16));
     const int grid = static_cast<int>(std::min<size_t>((work + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
-    bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(a);
+    bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(pa);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -659,7 +704,7 @@ cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const BwdArg
   if (stages & kStageDq) {
     const size_t n8 = static_cast<size_t>(a.BH) * a.N * D / 8;
     const int grid = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
-    dq_convert_kernel<<<grid, 256, 0, stream>>>(a, n8);
+    dq_convert_kernel<D><<<grid, 256, 0, stream>>>(qa, n8);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -678,42 +723,61 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
                        void* dv, void* workspace, int stages, cudaStream_t stream) {
   const int BH = p.B * p.H;
   CUtensorMap maps[4];
-  if ((stages & kStageDkdv) &&
-      (!make_tile_map(&maps[0], q, BH, p.N, p.d) || !make_tile_map(&maps[1], k, BH, p.N, p.d) ||
-       !make_tile_map(&maps[2], v, BH, p.N, p.d) || !make_tile_map(&maps[3], dO, BH, p.N, p.d)))
+  if ((stages & kStageDkdv) && (!make_tile_map(&maps[0], q, p.B, p.H, p.N, p.d, p.st[kQ]) ||
+                                 !make_tile_map(&maps[1], k, p.B, p.H, p.N, p.d, p.st[kK]) ||
+                                 !make_tile_map(&maps[2], v, p.B, p.H, p.N, p.d, p.st[kV]) ||
+                                 !make_tile_map(&maps[3], dO, p.B, p.H, p.N, p.d, p.st[kdO])))
     return cudaErrorInvalidValue;
+  const int n_tiles = (p.N + kTile - 1) / kTile;
+  const Workspace ws{static_cast<float*>(workspace)};
+  PreArgs pa;
+  pa.o = static_cast<const __nv_bfloat16*>(o);
+  pa.dO = static_cast<const __nv_bfloat16*>(dO);
+  pa.lse = lse;
+  pa.ws = ws;
+  pa.so = p.st[kO];
+  pa.sdo = p.st[kdO];
+  pa.N = p.N;
+  pa.H = p.H;
+  pa.Npad = n_tiles * kTile;
+  pa.BH = BH;
   BwdArgs a;
-  a.n_tiles = (p.N + kTile - 1) / kTile;
-  a.Npad = a.n_tiles * kTile;
-  a.N = p.N;
-  a.BH = BH;
-  a.n_items = BH * a.n_tiles;
-  a.o = static_cast<const __nv_bfloat16*>(o);
-  a.dO = static_cast<const __nv_bfloat16*>(dO);
-  a.lse = lse;
-  float* ws = static_cast<float*>(workspace);
-  a.Drow = ws;
-  a.lse2 = ws + static_cast<size_t>(BH) * a.Npad;
-  a.dq_acc = ws + 2 * static_cast<size_t>(BH) * a.Npad;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.ws = ws;
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.status = p.status;
+  a.N = p.N;
+  a.H = p.H;
+  a.Npad = n_tiles * kTile;
+  a.BH = BH;
+  a.n_tiles = n_tiles;
+  a.n_items = BH * n_tiles;
   a.scale = p.scale;
   a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.sdk = p.st[kdK];
+  a.sdv = p.st[kdV];
+  DqArgs qa;
+  qa.ws = ws;
+  qa.dq = static_cast<__nv_bfloat16*>(dq);
+  qa.sdq = p.st[kdQ];
+  qa.N = p.N;
+  qa.H = p.H;
+  qa.Npad = n_tiles * kTile;
+  qa.BH = BH;
+  qa.scale = p.scale;
   switch (p.d) {
     case 32:
-      return p.causal ? launch_bwd_t<32, true>(p, maps, a, stages, stream)
-                      : launch_bwd_t<32, false>(p, maps, a, stages, stream);
+      return p.causal ? launch_bwd_t<32, true>(p, maps, pa, a, qa, stages, stream)
+                      : launch_bwd_t<32, false>(p, maps, pa, a, qa, stages, stream);
     case 64:
-      return p.causal ? launch_bwd_t<64, true>(p, maps, a, stages, stream)
-                      : launch_bwd_t<64, false>(p, maps, a, stages, stream);
+      return p.causal ? launch_bwd_t<64, true>(p, maps, pa, a, qa, stages, stream)
+                      : launch_bwd_t<64, false>(p, maps, pa, a, qa, stages, stream);
     case 96:
-      return p.causal ? launch_bwd_t<96, true>(p, maps, a, stages, stream)
-                      : launch_bwd_t<96, false>(p, maps, a, stages, stream);
+      return p.causal ? launch_bwd_t<96, true>(p, maps, pa, a, qa, stages, stream)
+                      : launch_bwd_t<96, false>(p, maps, pa, a, qa, stages, stream);
     default:
-      return p.causal ? launch_bwd_t<128, true>(p, maps, a, stages, stream)
-                      : launch_bwd_t<128, false>(p, maps, a, stages, stream);
+      return p.causal ? launch_bwd_t<128, true>(p, maps, pa, a, qa, stages, stream)
+                      : launch_bwd_t<128, false>(p, maps, pa, a, qa, stages, stream);
   }
 }
 

@@ -93,8 +93,9 @@ struct FwdArgs {
   __nv_bfloat16* o;
   float* lse;
   int* status;
-  int N, BH, n_tiles, n_pairs, n_items;
+  int N, H, BH, n_tiles, n_pairs, n_items;
   float scale, scale_log2;
+  Strides so;  // element strides of o
 };
 
 __device__ __forceinline__ void decode_item(int item, const FwdArgs& a, bool causal, int& bh,
@@ -172,6 +173,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (item >= a.n_items) break;  // only in the last, partial round
         int bh, pair;
         decode_item(item, a, CAUSAL, bh, pair);
+        const int hh = bh % a.H, bb = bh / a.H;
         const int J = max(tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL));
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -181,8 +183,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint32_t bar = smem_u32(&bars->q_full[t]);
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
           for (int cb = 0; cb < Cfg::kColBlocks; ++cb)
-            tma_load_3d(sQ + (t * Cfg::kColBlocks + cb) * kBlockBytes, &tmQ, bar, 64 * cb,
-                        (2 * pair + t) * kTile, bh, pol_q);
+            tma_load_4d(sQ + (t * Cfg::kColBlocks + cb) * kBlockBytes, &tmQ, bar, 64 * cb,
+                        (2 * pair + t) * kTile, hh, bb, pol_q);
           ++q_issued[t];
         }
         for (int j = 0; j < J && ok; ++j) {
@@ -194,8 +196,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const uint32_t bar = smem_u32(&bars->kv_full[s]);
             mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
             for (int cb = 0; cb < Cfg::kColBlocks; ++cb)
-              tma_load_3d(sKV + (s * Cfg::kColBlocks + cb) * kBlockBytes, w ? &tmV : &tmK, bar,
-                          64 * cb, j * kTile, bh, pol_kv);
+              tma_load_4d(sKV + (s * Cfg::kColBlocks + cb) * kBlockBytes, w ? &tmV : &tmK, bar,
+                          64 * cb, j * kTile, hh, bb, pol_kv);
             ++kv_it;
           }
         }
@@ -439,7 +441,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int row = qt * kTile + r;
       const bool store = row < a.N;
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.N + row) * D;
+      __nv_bfloat16* orow = a.o + (bh / a.H) * a.so.batch + (bh % a.H) * a.so.head +
+                            static_cast<int64_t>(row) * a.so.row;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -487,11 +490,14 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const voi
                        float* lse, cudaStream_t stream) {
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
-  if (!make_tile_map(&mq, q, BH, p.N, p.d) || !make_tile_map(&mk, k, BH, p.N, p.d) ||
-      !make_tile_map(&mv, v, BH, p.N, p.d))
+  if (!make_tile_map(&mq, q, p.B, p.H, p.N, p.d, p.st[kQ]) ||
+      !make_tile_map(&mk, k, p.B, p.H, p.N, p.d, p.st[kK]) ||
+      !make_tile_map(&mv, v, p.B, p.H, p.N, p.d, p.st[kV]))
     return cudaErrorInvalidValue;
   FwdArgs a;
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.so = p.st[kO];
+  a.H = p.H;
   a.lse = lse;
   a.status = p.status;
   a.N = p.N;

@@ -84,7 +84,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   int num_sms = 0;
   int* status = nullptr;
   if (fa::current_device_setup(&num_sms, &status) != cudaSuccess) return FA_ERR_CUDA;
-  fa::Problem p{B, H, N, d, causal ? 1 : 0, scale, num_sms, status};
+  fa::Problem p{B, H, N, d, causal ? 1 : 0, scale, num_sms, status, {}};
+  for (int t = 0; t < fa::kNumTensors; ++t) p.st[t] = fa::contiguous_strides(H, N, d);
   const cudaError_t e = fa::launch_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, scratch,
                                        fa::kStagesAll, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

@@ -11,6 +11,15 @@ namespace fa {
 
 constexpr int kTile = 128;  // query rows per Q tile and keys per K/V tile
 
+// Element strides of one [B, H, N, d] tensor between batches, heads and rows;
+// the d values of a row are contiguous.
+struct Strides {
+  int64_t batch, head, row;
+};
+
+// Tensors of a call, in this order in Problem::st.
+enum TensorId : int { kQ = 0, kK, kV, kO, kdO, kdQ, kdK, kdV, kNumTensors };
+
 // Everything a launcher needs besides the tensor pointers.
 struct Problem {
   int B, H, N, d;
@@ -18,11 +27,18 @@ struct Problem {
   float scale;
   int num_sms;
   int* status;  // device address of the status word
+  Strides st[kNumTensors];
 };
 
-// Encodes a 3-D TMA map over a [B*H, N, d] bf16 tensor with a {64, 128, 1}
-// box and 128-byte swizzle. Returns false on failure.
-bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d);
+// Contiguous [B, H, N, d] strides.
+inline Strides contiguous_strides(int H, int N, int d) {
+  return Strides{static_cast<int64_t>(H) * N * d, static_cast<int64_t>(N) * d, d};
+}
+
+// Encodes a 4-D TMA map (d, N, H, B) over a bf16 tensor with the given
+// strides, a {64, 128, 1, 1} box and 128-byte swizzle. Returns false on failure.
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
+                   const Strides& s);
 
 // Launchers; they return a cudaError_t from the launch.
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,

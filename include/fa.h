@@ -69,6 +69,19 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int N, int d, int causal, float scale, void* stream);
 
 /*
+ * fa_fwd for tensors in any layout whose rows hold d contiguous values, such
+ * as [B, N, H, d] or K and V packed in one [B, N, 2, H, d] buffer (the
+ * "Flash Attention v2" notes, "Migration from v1 to v2": the packed-KV
+ * variant of the API). strides: 12 element strides, (batch, head, row) for
+ * q, k, v and o in that order; each a positive multiple of 8 (16 bytes).
+ * lse stays a contiguous fp32 [B, H, N] array. Results are those of fa_fwd
+ * on the same values.
+ */
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, const long long* strides, int causal, float scale,
+                         void* stream);
+
+/*
  * Size in bytes of the device workspace fa_bwd needs for these sizes: an
  * fp32 [B,H,N] row term D and an fp32 [B,H,N,d] dQ accumulator. Returns 0
  * for arguments fa_bwd would reject.
@@ -91,6 +104,16 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd for strided tensors (see fa_fwd_strided). strides: 24 element
+ * strides, (batch, head, row) for q, k, v, o, dO, dq, dk, dv in that order;
+ * each a positive multiple of 8. lse and the workspace are as for fa_bwd.
+ */
+fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, const long long* strides, int causal, float scale,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The three stages fa_bwd runs, in this order, for callers that schedule or

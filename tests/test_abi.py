@@ -125,3 +125,20 @@ def test_library_has_no_torch_dependency(lib):
 def test_exp2_selftest_rejects_before_launch(lib):
     assert lib.fa_selftest_exp2(None, P, 4, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_selftest_exp2(P, P, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_strided_entry_points_reject_bad_strides(lib):
+    import ctypes
+    good = [4 * 8 * 64, 8 * 64, 64] * 8
+    for bad in (0, -8, 12, 1 << 36):
+        st = list(good)
+        st[4] = bad
+        arr = (ctypes.c_longlong * 24)(*st)
+        assert lib.fa_fwd_strided(P, P, P, P, P, 1, 4, 8, 64, arr, 0, 0.125, None) == \
+            fa.FA_ERR_INVALID_ARG
+        assert lib.fa_bwd_strided(*([P] * 9), 1, 4, 8, 64, arr, 0, 0.125, P, 1 << 20, None) == \
+            fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_strided(P, P, P, P, P, 1, 4, 8, 64, None, 0, 0.125, None) == \
+        fa.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_strided(*([P] * 9), 1, 4, 8, 64, None, 0, 0.125, P, 1 << 20, None) == \
+        fa.FA_ERR_INVALID_ARG
