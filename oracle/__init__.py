@@ -11,4 +11,6 @@ from .attention import (  # noqa: F401
     head_backward,
     head_forward,
     head_probabilities,
+    varlen_backward,
+    varlen_forward,
 )

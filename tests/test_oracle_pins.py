@@ -31,6 +31,12 @@ def test_oracle_pin(check):
     assert ok, msg
 
 
+@pytest.mark.parametrize("check", pins.VARLEN_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_varlen_pin(check):
+    ok, msg = check(oracle.varlen_forward, oracle.varlen_backward)
+    assert ok, msg
+
+
 def test_rows_of_p_sum_to_one():
     for causal in (False, True):
         t = pins.rand_head(51, 45, 8)
@@ -95,6 +101,13 @@ def test_oracle_rejects_bad_arguments():
     t = pins.rand_head(61, 4, 2)
     with pytest.raises(ValueError):
         oracle.head_forward(t["q"], t["k"][:3], t["v"], False, 1.0)
+    with pytest.raises(ValueError):
+        oracle.head_forward(t["q"], t["k"][:, :1], t["v"][:, :1], False, 1.0)
+    x, cu_q, cu_k = pins.packed_inputs(62, [2, 3], [3, 1], 1, 2)
+    for bad_q, bad_k in (([0, 2, 4], cu_k), ([1, 2, 5], cu_k), ([0, 3, 2], cu_k),
+                         (cu_q, [0, 3])):
+        with pytest.raises(ValueError):
+            oracle.varlen_forward(x["q"], x["k"], x["v"], bad_q, bad_k, False, 1.0)
     with pytest.raises(ValueError):
         oracle.head_forward(t["q"], t["k"], t["v"], False, math.inf)
     with pytest.raises(ValueError):
