@@ -14,8 +14,11 @@ from .binding import (  # noqa: F401
     FaError,
     fa_bwd,
     fa_bwd_stages,
+    fa_bwd_varlen,
+    fa_bwd_varlen_workspace_size,
     fa_bwd_workspace_size,
     fa_fwd,
+    fa_fwd_varlen,
     fa_last_device_status,
     fa_selftest_exp2,
     fa_selftest_wait_timeout,

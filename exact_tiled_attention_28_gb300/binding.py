@@ -25,7 +25,8 @@ FA_ERR_WORKSPACE = 5
 EXPORTED = ("fa_abi_version", "fa_fwd", "fa_fwd_strided", "fa_bwd_workspace_size", "fa_bwd",
             "fa_bwd_strided", "fa_bwd_preprocess",
             "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout", "fa_selftest_exp2",
-            "fa_status_string", "fa_last_device_status")
+            "fa_status_string", "fa_last_device_status", "fa_fwd_nqnk", "fa_bwd_nqnk",
+            "fa_fwd_varlen", "fa_bwd_varlen_workspace_size", "fa_bwd_varlen")
 
 # fixed device scratch of fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in include/fa.h)
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -83,6 +84,16 @@ def load():
     lib.fa_status_string.argtypes = [i]
     lib.fa_last_device_status.restype = i
     lib.fa_last_device_status.argtypes = [vp]
+    lib.fa_fwd_nqnk.restype = i
+    lib.fa_fwd_nqnk.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ll, i, f, vp]
+    lib.fa_bwd_nqnk.restype = i
+    lib.fa_bwd_nqnk.argtypes = [vp] * 9 + [i, i, i, i, i, ll, i, f, vp, sz, vp]
+    lib.fa_fwd_varlen.restype = i
+    lib.fa_fwd_varlen.argtypes = [vp] * 7 + [i] * 7 + [ll, i, f, vp]
+    lib.fa_bwd_varlen_workspace_size.restype = sz
+    lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_varlen.restype = i
+    lib.fa_bwd_varlen.argtypes = [vp] * 11 + [i] * 7 + [ll, i, f, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -131,6 +142,12 @@ def _dev_ptr(t, name, dtype, shape, strided=False):
     elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
+
+
+def _check_workspace(workspace):
+    import torch
+    if not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
 
 
 def _strides(tensors):
@@ -207,17 +224,24 @@ def fa_last_device_status(stream=None) -> int:
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     """o, lse <- attention(q, k, v) on the current (or given) CUDA stream.
 
-    q, k, v, o are [B, H, N, d] bf16 views with a contiguous last dimension (a
-    [B, N, H, d] tensor passed as .transpose(1, 2), or K and V slices of one
-    packed buffer, go through fa_fwd_strided); lse is contiguous fp32 [B, H, N]."""
+    q, o are [B, H, Nq, d] and k, v [B, H, Nk, d] bf16 views with a contiguous
+    last dimension (a [B, N, H, d] tensor passed as .transpose(1, 2), or K and
+    V slices of one packed buffer, go through the strided entry points); lse
+    is contiguous fp32 [B, H, Nq]. Nq != Nk goes through fa_fwd_nqnk (causal
+    mask aligned at the bottom right)."""
     import torch
     B, H, N, d = _shape(q)
+    Nk = int(k.shape[2]) if k.dim() == 4 else -1
     bf = torch.bfloat16
     ts = ((q, "q"), (k, "k"), (v, "v"), (o, "o"))
-    args = [_dev_ptr(t, n, bf, (B, H, N, d), strided=True) for t, n in ts]
+    args = [_dev_ptr(t, n, bf, (B, H, Nk if n in ("k", "v") else N, d), strided=True)
+            for t, n in ts]
     args.append(_dev_ptr(lse, "lse", torch.float32, (B, H, N)))
     st = _strides([t for t, _ in ts])
-    if st is None:
+    if Nk != N:
+        _check(load().fa_fwd_nqnk(*args, B, H, N, Nk, d, st, int(bool(causal)), float(scale),
+                                  _stream_handle(stream)), "fa_fwd_nqnk")
+    elif st is None:
         _check(fa_fwd_raw(*args, B, H, N, d, causal, scale, _stream_handle(stream)), "fa_fwd")
     else:
         _check(load().fa_fwd_strided(*args, B, H, N, d, st, int(bool(causal)), float(scale),
@@ -227,18 +251,24 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
 def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace,
            stream=None) -> None:
     """dq, dk, dv <- gradients of sum(o * do); workspace is a CUDA uint8 tensor of at
-    least fa_bwd_workspace_size(B, H, N, d) bytes."""
+    least fa_bwd_workspace_size(B, H, Nq, d) bytes. Shapes as for fa_fwd (dk, dv
+    like k, dq and do like q)."""
     import torch
     B, H, N, d = _shape(q)
+    Nk = int(k.shape[2]) if k.dim() == 4 else -1
     bf = torch.bfloat16
     ts = ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))
-    p = {n: _dev_ptr(t, n, bf, (B, H, N, d), strided=True) for t, n in ts}
+    p = {n: _dev_ptr(t, n, bf, (B, H, Nk if n in ("k", "v", "dk", "dv") else N, d), strided=True)
+         for t, n in ts}
     pl = _dev_ptr(lse, "lse", torch.float32, (B, H, N))
-    if not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
-        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    _check_workspace(workspace)
     ptrs = [p["q"], p["k"], p["v"], p["o"], pl, p["do"], p["dq"], p["dk"], p["dv"]]
     st = _strides([t for t, _ in ts])
-    if st is None:
+    if Nk != N:
+        _check(load().fa_bwd_nqnk(*ptrs, B, H, N, Nk, d, st, int(bool(causal)), float(scale),
+                                  workspace.data_ptr(), workspace.numel(),
+                                  _stream_handle(stream)), "fa_bwd_nqnk")
+    elif st is None:
         _check(fa_bwd_raw(*ptrs, B, H, N, d, causal, scale, workspace.data_ptr(),
                           workspace.numel(), _stream_handle(stream)), "fa_bwd")
     else:
@@ -292,3 +322,76 @@ def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float,
              for t, n in ((do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))]
     _check(fa_bwd_noalloc_raw(*ptrs, B, H, N, d, causal, scale, _stream_handle(stream)),
            "fa_bwd_noalloc")
+
+
+# ---------------------------------------------------------------------------
+# packed batches of variable-length sequences
+
+def fa_bwd_varlen_workspace_size(B: int, H: int, total_q: int, d: int) -> int:
+    return int(load().fa_bwd_varlen_workspace_size(B, H, total_q, d))
+
+
+def _varlen_args(q, k, v, tensors_q, tensors_k, cu_seqlens_q, cu_seqlens_k):
+    """Pointers, sizes and (head, row) strides of packed [T, H, d] views."""
+    import torch
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("expected packed [T, H, d] tensors")
+    Tq, H, d = (int(x) for x in q.shape)
+    Tk = int(k.shape[0])
+    bf = torch.bfloat16
+    ptrs = {}
+    for t, n in tensors_q:
+        ptrs[n] = _dev_ptr(t, n, bf, (Tq, H, d), strided=True)
+    for t, n in tensors_k:
+        ptrs[n] = _dev_ptr(t, n, bf, (Tk, H, d), strided=True)
+    B = int(cu_seqlens_q.numel()) - 1
+    for c, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        _dev_ptr(c, n, torch.int32, (B + 1,))
+    order = list(tensors_q[:1]) + list(tensors_k) + list(tensors_q[1:])
+    return Tq, Tk, H, d, B, ptrs, order
+
+
+def _varlen_strides(tensors):
+    if all(t.is_contiguous() for t in tensors):
+        return None
+    vals = []
+    for t in tensors:
+        vals += [int(t.stride(1)), int(t.stride(0))]
+    return (ctypes.c_longlong * len(vals))(*vals)
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, causal: bool, scale: float, stream=None) -> None:
+    """o, lse <- attention of a packed batch: q, o [total_q, H, d] and k, v
+    [total_k, H, d] bf16 views with a contiguous last dimension; cu_seqlens_q,
+    cu_seqlens_k int32 CUDA tensors of B + 1 prefix offsets; lse fp32
+    [H, total_q]. Causal masks are aligned at the bottom right per sequence."""
+    import torch
+    Tq, Tk, H, d, B, p, _ = _varlen_args(q, k, v, ((q, "q"), (o, "o")), ((k, "k"), (v, "v")),
+                                         cu_seqlens_q, cu_seqlens_k)
+    pl = _dev_ptr(lse, "lse", torch.float32, (H, Tq))
+    st = _varlen_strides([q, k, v, o])
+    _check(load().fa_fwd_varlen(p["q"], p["k"], p["v"], p["o"], pl, cu_seqlens_q.data_ptr(),
+                                cu_seqlens_k.data_ptr(), B, H, Tq, Tk, int(max_seqlen_q),
+                                int(max_seqlen_k), d, st, int(bool(causal)), float(scale),
+                                _stream_handle(stream)), "fa_fwd_varlen")
+
+
+def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
+                  max_seqlen_q: int, max_seqlen_k: int, causal: bool, scale: float, workspace,
+                  stream=None) -> None:
+    """dq, dk, dv <- gradients of sum(o * do) for a packed batch (see
+    fa_fwd_varlen); workspace is a CUDA uint8 tensor of at least
+    fa_bwd_varlen_workspace_size(B, H, total_q, d) bytes."""
+    import torch
+    Tq, Tk, H, d, B, p, _ = _varlen_args(
+        q, k, v, ((q, "q"), (o, "o"), (do, "do"), (dq, "dq")),
+        ((k, "k"), (v, "v"), (dk, "dk"), (dv, "dv")), cu_seqlens_q, cu_seqlens_k)
+    pl = _dev_ptr(lse, "lse", torch.float32, (H, Tq))
+    _check_workspace(workspace)
+    st = _varlen_strides([q, k, v, o, do, dq, dk, dv])
+    _check(load().fa_bwd_varlen(p["q"], p["k"], p["v"], p["o"], pl, p["do"], p["dq"], p["dk"],
+                                p["dv"], cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, H,
+                                Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), d, st,
+                                int(bool(causal)), float(scale), workspace.data_ptr(),
+                                workspace.numel(), _stream_handle(stream)), "fa_bwd_varlen")

@@ -99,6 +99,22 @@ __global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
   mbar_wait(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
 }
 
+// Checks a packed batch's sequence offsets (see launch_varlen_check).
+__global__ void varlen_check_kernel(const int* cu_q, const int* cu_k, int B, int rows_q,
+                                    int rows_k, int max_q, int max_k, int* status) {
+  bool bad = false;
+  for (int b = threadIdx.x; b <= B; b += blockDim.x) {
+    const long long q = cu_q[b], k = cu_k[b];
+    if (b == 0 && (q != 0 || k != 0)) bad = true;
+    if (b == B && (q != rows_q || k != rows_k)) bad = true;
+    if (b < B) {
+      const long long nq = cu_q[b + 1] - q, nk = cu_k[b + 1] - k;
+      if (nq < 0 || nk < 0 || nq > max_q || nk > max_k) bad = true;
+    }
+  }
+  if (bad) atomicCAS(status, DEV_OK, DEV_BADARG);
+}
+
 // Evaluates the forward kernel's FMA-pipe exp2 on n inputs.
 __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -121,6 +137,12 @@ cudaError_t current_device_setup(int* num_sms, int** status) {
   *num_sms = di.num_sms;
   *status = di.status;
   return cudaSuccess;
+}
+
+cudaError_t launch_varlen_check(const Problem& p, cudaStream_t stream) {
+  varlen_check_kernel<<<1, 256, 0, stream>>>(p.cu_q, p.cu_k, p.B, p.rows_q, p.rows_k, p.max_q,
+                                             p.max_k, p.status);
+  return cudaGetLastError();
 }
 
 bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
@@ -270,6 +292,168 @@ fa_status fa_bwd_dq_finalize(void* dq, int B, int H, int N, int d, float scale, 
                     H, N, d, 0, scale, workspace, workspace_bytes, fa::kStageDq, {dq}, stream);
 }
 
+namespace {
+
+// Work items of the var kernels must fit an int: sequences x heads x the
+// longest sequence's tiles.
+bool var_items_fit(int B, int H, int max_q, int max_k) {
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  return bh * ((max_q + 255) / 256) < (int64_t(1) << 31) &&
+         bh * ((max_k + 127) / 128) < (int64_t(1) << 31);
+}
+
+// Problem for B dense sequences of Nq query and Nk key rows; strides: 3 per
+// tensor (batch, head, row) in TensorId order for n tensors, or null.
+fa_status nqnk_problem(fa::Problem* p, int B, int H, int Nq, int Nk, int d,
+                       const long long* strides, int n, int causal, float scale) {
+  fa_status s = fa::check_sizes(B, H, Nq, d, scale);
+  if (s != FA_OK) return s;
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  if (!var_items_fit(B, H, Nq, Nk)) return FA_ERR_UNSUPPORTED;
+  if (strides != nullptr) {
+    s = fa::check_strides(strides, n);
+    if (s != FA_OK) return s;
+  }
+  *p = fa::Problem{B, H, Nq, d, causal ? 1 : 0, scale, 0, nullptr, {}};
+  for (int t = 0; t < fa::kNumTensors; ++t) {
+    const bool kv = t == fa::kK || t == fa::kV || t == fa::kdK || t == fa::kdV;
+    p->st[t] = (strides != nullptr && t < n)
+                   ? fa::Strides{strides[3 * t], strides[3 * t + 1], strides[3 * t + 2]}
+                   : fa::contiguous_strides(H, kv ? Nk : Nq, d);
+  }
+  p->var = 1;
+  p->Nk = Nk;
+  p->rows_q = p->max_q = Nq;
+  p->rows_k = p->max_k = Nk;
+  return FA_OK;
+}
+
+// Problem for a packed batch; strides: 2 per tensor (head, row) for n
+// tensors, or null for [T, H, d] tensors.
+fa_status varlen_problem(fa::Problem* p, const int* cu_q, const int* cu_k, int B, int H,
+                         int total_q, int total_k, int max_q, int max_k, int d,
+                         const long long* strides, int n, int causal, float scale) {
+  fa_status s = fa::check_sizes(B, H, total_q, d, scale);
+  if (s != FA_OK) return s;
+  if (total_k < 1 || max_q < 1 || max_k < 1 || cu_q == nullptr || cu_k == nullptr ||
+      (reinterpret_cast<uintptr_t>(cu_q) & 3u) != 0 || (reinterpret_cast<uintptr_t>(cu_k) & 3u) != 0)
+    return FA_ERR_INVALID_ARG;
+  if (!var_items_fit(B, H, max_q, max_k)) return FA_ERR_UNSUPPORTED;
+  long long st[3 * fa::kNumTensors];
+  for (int t = 0; t < fa::kNumTensors; ++t) {
+    const long long head = strides != nullptr && t < n ? strides[2 * t] : d;
+    const long long row = strides != nullptr && t < n ? strides[2 * t + 1] : static_cast<long long>(H) * d;
+    const bool kv = t == fa::kK || t == fa::kV || t == fa::kdK || t == fa::kdV;
+    st[3 * t] = row * (kv ? total_k : total_q);  // one batch coordinate: the whole buffer
+    st[3 * t + 1] = head;
+    st[3 * t + 2] = row;
+  }
+  s = fa::check_strides(st, n);
+  if (s != FA_OK) return s;
+  *p = fa::Problem{B, H, max_q, d, causal ? 1 : 0, scale, 0, nullptr, {}};
+  for (int t = 0; t < fa::kNumTensors; ++t) p->st[t] = fa::Strides{st[3 * t], st[3 * t + 1], st[3 * t + 2]};
+  p->var = 1;
+  p->Nk = max_k;
+  p->cu_q = cu_q;
+  p->cu_k = cu_k;
+  p->rows_q = total_q;
+  p->rows_k = total_k;
+  p->max_q = max_q;
+  p->max_k = max_k;
+  return FA_OK;
+}
+
+// The device facts a Problem built from the arguments alone still lacks.
+bool add_device(fa::Problem* p) {
+  fa::DeviceInfo di;
+  if (fa::device_info(&di) != cudaSuccess) return false;
+  p->num_sms = di.num_sms;
+  p->status = di.status;
+  return true;
+}
+
+fa_status var_fwd(fa::Problem p, const void* q, const void* k, const void* v, void* o,
+                  float* lse, void* stream) {
+  if (!add_device(&p)) return FA_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.cu_q != nullptr && fa::launch_varlen_check(p, st) != cudaSuccess) return FA_ERR_CUDA;
+  return fa::launch_fwd(p, q, k, v, o, lse, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status var_bwd(fa::Problem p, const void* q, const void* k, const void* v,
+                  const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || !fa::aligned16(workspace) ||
+      workspace_bytes < fa::bwd_var_workspace_bytes(p.cu_q != nullptr, p.B, p.H, p.rows_q, p.d))
+    return FA_ERR_WORKSPACE;
+  if (!add_device(&p)) return FA_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.cu_q != nullptr && fa::launch_varlen_check(p, st) != cudaSuccess) return FA_ERR_CUDA;
+  return fa::launch_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, workspace, fa::kStagesAll, st) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status fa_fwd_nqnk(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, const long long* strides, int causal,
+                      float scale, void* stream) {
+  fa::Problem p;
+  fa_status s = nqnk_problem(&p, B, H, Nq, Nk, d, strides, 4, causal, scale);
+  if (s != FA_OK) return s;
+  s = fa::check_ptrs({q, k, v, o, lse});
+  if (s != FA_OK) return s;
+  return var_fwd(p, q, k, v, o, lse, stream);
+}
+
+fa_status fa_bwd_nqnk(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                      int H, int Nq, int Nk, int d, const long long* strides, int causal,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  fa::Problem p;
+  fa_status s = nqnk_problem(&p, B, H, Nq, Nk, d, strides, fa::kNumTensors, causal, scale);
+  if (s != FA_OK) return s;
+  s = fa::check_ptrs({q, k, v, o, lse, dO, dq, dk, dv});
+  if (s != FA_OK) return s;
+  return var_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                        const long long* strides, int causal, float scale, void* stream) {
+  fa::Problem p;
+  fa_status s = varlen_problem(&p, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                               max_seqlen_q, max_seqlen_k, d, strides, 4, causal, scale);
+  if (s != FA_OK) return s;
+  s = fa::check_ptrs({q, k, v, o, lse});
+  if (s != FA_OK) return s;
+  return var_fwd(p, q, k, v, o, lse, stream);
+}
+
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int d) {
+  if (fa::check_sizes(B, H, total_q, d, 1.f) != FA_OK) return 0;
+  return fa::bwd_var_workspace_bytes(true, B, H, total_q, d);
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                        const long long* strides, int causal, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  fa::Problem p;
+  fa_status s = varlen_problem(&p, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                               max_seqlen_q, max_seqlen_k, d, strides, fa::kNumTensors, causal,
+                               scale);
+  if (s != FA_OK) return s;
+  s = fa::check_ptrs({q, k, v, o, lse, dO, dq, dk, dv});
+  if (s != FA_OK) return s;
+  return var_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
 fa_status fa_selftest_wait_timeout(int limit_ms, void* stream) {
   if (limit_ms < 1 || limit_ms > 2000) return FA_ERR_INVALID_ARG;
   fa::DeviceInfo di;
@@ -297,7 +481,7 @@ fa_status fa_last_device_status(void* stream) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(fa::g_device_status, &zero, sizeof(int)) != cudaSuccess)
       return FA_ERR_CUDA;
-    return FA_ERR_TIMEOUT;
+    return h == fa::DEV_BADARG ? FA_ERR_INVALID_ARG : FA_ERR_TIMEOUT;
   }
   return FA_OK;
 }

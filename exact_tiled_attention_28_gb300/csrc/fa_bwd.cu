@@ -41,6 +41,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "schedule.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -137,6 +138,42 @@ struct BwdArgs {
 };
 static_assert(sizeof(BwdArgs) == 112, "dK/dV argument struct grew");
 
+// Sequences of unequal lengths (dense or packed batch; sh = b * H + h runs
+// over sequences and heads). The workspace holds D and lse2 as
+// [planes, lpad] (each sequence's rows from its Seq::pst on, whole 128-row
+// tiles, pad rows D = 0 and lse2 = +inf), then the fp32 accumulator
+// [planes, rows_q, d]; planes = batch coordinates x H.
+struct PreVarArgs {
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dO;
+  const float* lse;  // [planes, rows_q]
+  float* ws;
+  Strides so, sdo;
+  int planes, lpad, max_q_pad, BH;
+  VarGeom g;
+};
+
+struct BwdVarArgs {
+  float* ws;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  int BH, n_tiles, n_items;  // n_tiles: key tiles of the longest sequence
+  int planes, lpad;
+  float scale, scale_log2;
+  Strides sdk, sdv;
+  VarGeom g;
+};
+
+template <bool VAR>
+struct BwdArgsOf {
+  using type = BwdArgs;
+};
+template <>
+struct BwdArgsOf<true> {
+  using type = BwdVarArgs;
+};
+
 // Element offset of row `row` of head bh (= b * H + h) in a strided tensor.
 __device__ __forceinline__ int64_t row_offset(const Strides& st, int bh, int H, int row) {
   return (bh / H) * st.batch + (bh % H) * st.head + static_cast<int64_t>(row) * st.row;
@@ -193,6 +230,65 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
   }
 }
 
+// The pre-pass for sequences of unequal lengths: one unit per (sequence,
+// head, row r < roundup(max_q, 128)); rows past the sequence's padded length
+// do nothing. A row whose forward saw no key (LSE = -inf) gets lse2 = +inf,
+// so that its P is 0 and it adds nothing to any gradient.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_var_kernel(const PreVarArgs a) {
+  constexpr int kLanesPerRow = D <= 32 ? 4 : (D <= 64 ? 8 : 16);
+  constexpr int kActive = D / 8;
+  const size_t units = static_cast<size_t>(a.BH) * a.max_q_pad;
+  float* const Drow = a.ws;
+  float* const lse2 = a.ws + static_cast<size_t>(a.planes) * a.lpad;
+  float* const dq_acc = a.ws + 2 * static_cast<size_t>(a.planes) * a.lpad;
+  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       g < units * kLanesPerRow; g += nthreads) {
+    const size_t unit = g / kLanesPerRow;
+    const int part = static_cast<int>(g % kLanesPerRow);
+    const int sh = static_cast<int>(unit / a.max_q_pad);
+    const int r = static_cast<int>(unit % a.max_q_pad);
+    const Seq sq = seq_of(sh, a.g);
+    const size_t plane = static_cast<size_t>(sq.bb) * a.g.H + sq.hh;
+    const bool real = r < sq.nq;
+    const bool padded = r < (sq.nq + kTile - 1) / kTile * kTile;
+    float dot = 0.f;
+    if (real && part < kActive) {
+      const int64_t row = sq.q0 + r;
+      const uint4 ov = *reinterpret_cast<const uint4*>(a.o + sq.bb * a.so.batch + sq.hh * a.so.head +
+                                                       row * a.so.row + part * 8);
+      const uint4 gv = *reinterpret_cast<const uint4*>(
+          a.dO + sq.bb * a.sdo.batch + sq.hh * a.sdo.head + row * a.sdo.row + part * 8);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 of = __bfloat1622float2(o2[u]);
+        const float2 gf = __bfloat1622float2(g2[u]);
+        dot = fmaf(of.x, gf.x, dot);
+        dot = fmaf(of.y, gf.y, dot);
+      }
+      float4* z = reinterpret_cast<float4*>(dq_acc + (plane * a.g.rows_q + row) * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+      dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (part == 0 && padded) {
+      const size_t idx = plane * a.lpad + sq.pst + r;
+      float l2 = __int_as_float(0x7f800000);
+      if (real) {
+        const float lse = a.lse[plane * a.g.rows_q + sq.q0 + r];
+        if (lse != __int_as_float(0xff800000)) l2 = lse * 1.4426950408889634f;
+      }
+      Drow[idx] = dot;
+      lse2[idx] = l2;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 3. dq = bf16(scale * accumulator)
 
@@ -218,7 +314,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const DqArgs a, size_t 
 // ---------------------------------------------------------------------------
 // 2. dK / dV (and dQ contributions)
 
-__device__ __forceinline__ void decode_kv_item(int item, const BwdArgs& a, bool causal, int& bh,
+template <class Args>
+__device__ __forceinline__ void decode_kv_item(int item, const Args& a, bool causal, int& bh,
                                                int& j) {
   if (causal) {  // key block 0 visits every query block: longest first
     j = item / a.BH;
@@ -239,6 +336,36 @@ __device__ __forceinline__ int qblock_at(int j, int u, int n_q, bool causal) {
   return i < n_q ? i : i - n_q;
 }
 
+// Query blocks that key block j of a sequence of unequal lengths visits:
+// causal, the blocks from the first one holding a query that sees key
+// j * 128 (bottom-right alignment) to the last; otherwise all of them,
+// starting at j mod n_q. n_it = 0 when the key block lies past the sequence
+// or the sequence has no queries.
+struct KvWork {
+  int n_it, i0, rot, n_q;
+};
+
+__device__ __forceinline__ KvWork var_kv_work(int j, const Seq& sq, bool causal) {
+  KvWork w{0, 0, 0, 0};
+  if (sq.nq <= 0 || j * kTile >= sq.nk) return w;
+  w.n_q = (sq.nq + kTile - 1) / kTile;
+  if (causal) {
+    const int first = j * kTile - (sq.nk - sq.nq);
+    w.i0 = first > 0 ? first / kTile : 0;
+    w.n_it = w.n_q - w.i0;
+  } else {
+    w.rot = j % w.n_q;
+    w.n_it = w.n_q;
+  }
+  return w;
+}
+
+__device__ __forceinline__ int var_qblock(const KvWork& w, int u, bool causal) {
+  if (causal) return w.i0 + u;
+  const int i = w.rot + u;
+  return i < w.n_q ? i : i - w.n_q;
+}
+
 __device__ __forceinline__ void cp_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                             uint32_t bar) {
   asm volatile(
@@ -256,11 +383,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // holds one warp of every warpgroup: 4 x 32 x 128 = 16384). The warpgroups then
 // rebalance with setmaxnreg: compute 128, dQ readout 176, load/MMA 80; per
 // sub-partition 128 + 128 + 176 + 80 = 512 registers per lane, the launch total.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VAR>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const BwdArgs a) {
+                    const typename BwdArgsOf<VAR>::type a) {
   using Cfg = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
@@ -277,7 +404,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_q = a.n_tiles;
+  const int n_q = a.n_tiles;  // VAR: key tiles of the longest sequence (unused as query blocks)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->kv_full), 1);
@@ -326,21 +453,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (item >= a.n_items) break;  // only in the last, partial round
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
-        const int hh = bh % a.H, bb = bh / a.H;
+        int hh, bb, q0 = 0, k0 = 0, n_it;
+        KvWork w;
+        size_t lrow = 0;  // VAR: first padded D / lse2 row of the sequence
+        if constexpr (VAR) {
+          const Seq sq = seq_of(bh, a.g);
+          w = var_kv_work(j, sq, CAUSAL);
+          if (w.n_it == 0) continue;
+          hh = sq.hh;
+          bb = sq.bb;
+          q0 = sq.q0;
+          k0 = sq.k0;
+          n_it = w.n_it;
+          lrow = (static_cast<size_t>(sq.bb) * a.g.H + sq.hh) * a.lpad + sq.pst;
+        } else {
+          hh = bh % a.H;
+          bb = bh / a.H;
+          n_it = CAUSAL ? n_q - j : n_q;
+        }
         ok = mbar_wait(smem_u32(&bars->kv_empty), (kv_round & 1) ^ 1, abort, a.status);
         if (!ok) break;
         {
           const uint32_t bar = smem_u32(&bars->kv_full);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           for (int cb = 0; cb < Cfg::kColBlocks; ++cb) {
-            tma_load_4d(sK + cb * kBlk, &tmK, bar, 64 * cb, j * kTile, hh, bb, pol_kv);
-            tma_load_4d(sV + cb * kBlk, &tmV, bar, 64 * cb, j * kTile, hh, bb, pol_kv);
+            tma_load_4d(sK + cb * kBlk, &tmK, bar, 64 * cb, k0 + j * kTile, hh, bb, pol_kv);
+            tma_load_4d(sV + cb * kBlk, &tmV, bar, 64 * cb, k0 + j * kTile, hh, bb, pol_kv);
           }
           ++kv_round;
         }
-        const int n_it = CAUSAL ? n_q - j : n_q;
         for (int u = 0; u < n_it && ok; ++u) {
-          const int i = qblock_at(j, u, n_q, CAUSAL);
+          int i;
+          if constexpr (VAR)
+            i = var_qblock(w, u, CAUSAL);
+          else
+            i = qblock_at(j, u, n_q, CAUSAL);
           const uint32_t s = st_it % Cfg::kStages;
           ok = mbar_wait(smem_u32(&bars->st_empty[s]), ((st_it / Cfg::kStages) & 1) ^ 1, abort,
                          a.status);
@@ -349,13 +496,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t st = sSt + s * Cfg::kStageBytes;
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes + 1024);
           for (int cb = 0; cb < Cfg::kColBlocks; ++cb) {
-            tma_load_4d(st + cb * kBlk, &tmQ, bar, 64 * cb, i * kTile, hh, bb, pol_q);
-            tma_load_4d(st + Cfg::kTileBytes + cb * kBlk, &tmdO, bar, 64 * cb, i * kTile, hh, bb,
-                        pol_q);
+            tma_load_4d(st + cb * kBlk, &tmQ, bar, 64 * cb, q0 + i * kTile, hh, bb, pol_q);
+            tma_load_4d(st + Cfg::kTileBytes + cb * kBlk, &tmdO, bar, 64 * cb, q0 + i * kTile, hh,
+                        bb, pol_q);
           }
-          const size_t roff = static_cast<size_t>(bh) * a.Npad + static_cast<size_t>(i) * kTile;
-          cp_bulk_g2s(st + 2 * Cfg::kTileBytes, a.ws.lse2(a.BH, a.Npad) + roff, 512, bar);
-          cp_bulk_g2s(st + 2 * Cfg::kTileBytes + 512, a.ws.Drow(a.BH, a.Npad) + roff, 512, bar);
+          if constexpr (VAR) {
+            const size_t roff = lrow + static_cast<size_t>(i) * kTile;
+            const size_t plane_rows = static_cast<size_t>(a.planes) * a.lpad;
+            cp_bulk_g2s(st + 2 * Cfg::kTileBytes, a.ws + plane_rows + roff, 512, bar);
+            cp_bulk_g2s(st + 2 * Cfg::kTileBytes + 512, a.ws + roff, 512, bar);
+          } else {
+            const size_t roff = static_cast<size_t>(bh) * a.Npad + static_cast<size_t>(i) * kTile;
+            cp_bulk_g2s(st + 2 * Cfg::kTileBytes, a.ws.lse2(a.BH, a.Npad) + roff, 512, bar);
+            cp_bulk_g2s(st + 2 * Cfg::kTileBytes + 512, a.ws.Drow(a.BH, a.Npad) + roff, 512, bar);
+          }
           ++st_it;
         }
       }
@@ -426,8 +580,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (item >= a.n_items) break;  // only in the last, partial round
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
-        const int i0 = CAUSAL ? j : 0;
-        const int n_it = n_q - i0;
+        int n_it;
+        if constexpr (VAR) {
+          n_it = var_kv_work(j, seq_of(bh, a.g), CAUSAL).n_it;
+          if (n_it == 0) {  // skipped by the loader too: no K/V round
+            --kv_round;
+            continue;
+          }
+        } else {
+          n_it = n_q - (CAUSAL ? j : 0);
+        }
         ok = mbar_wait(smem_u32(&bars->kv_full), kv_round & 1, abort, a.status);
         if (!ok) break;
         // prologue: S^T(0), dP^T(0); dP needs the dQ readout of the previous item done
@@ -504,10 +666,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (item >= a.n_items) break;  // only in the last, partial round
       int bh, j;
       decode_kv_item(item, a, CAUSAL, bh, j);
-      const int i0 = CAUSAL ? j : 0;
-      const int n_it = n_q - i0;
+      int n_it;
+      KvWork w;
+      int key_thr = 0;  // VAR: key row of this thread minus (nk - nq); >= 2^29 past nk
+      if constexpr (VAR) {
+        const Seq sq = seq_of(bh, a.g);
+        w = var_kv_work(j, sq, CAUSAL);
+        n_it = w.n_it;
+        const int key = j * kTile + r;
+        if (n_it == 0) {
+          if (sq.nq == 0 && key < sq.nk) {  // keys of a sequence without queries: dK = dV = 0
+            __nv_bfloat16* out = (wg == 0 ? a.dv : a.dk) +
+                                 sq.bb * (wg == 0 ? a.sdv.batch : a.sdk.batch) +
+                                 sq.hh * (wg == 0 ? a.sdv.head : a.sdk.head) +
+                                 static_cast<int64_t>(sq.k0 + key) * (wg == 0 ? a.sdv.row : a.sdk.row);
+            for (int c = 0; c < D; c += 8)
+              *reinterpret_cast<uint4*>(out + c) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          --kv_round;  // no K/V round for this item
+          continue;
+        }
+        key_thr = key >= sq.nk ? (1 << 29) : (CAUSAL ? key - (sq.nk - sq.nq) : -(1 << 29));
+      } else {
+        n_it = n_q - (CAUSAL ? j : 0);
+      }
       for (int u = 0; u < n_it; ++u, ++it, ++st_it) {
-        const int i = qblock_at(j, u, n_q, CAUSAL);
+        int i;
+        if constexpr (VAR)
+          i = var_qblock(w, u, CAUSAL);
+        else
+          i = qblock_at(j, u, n_q, CAUSAL);
         const uint32_t s = st_it % Cfg::kStages;
         const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kOffStages +
                                                            s * Cfg::kStageBytes +
@@ -519,8 +707,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         uint32_t sr[64];
         tmem_ld64(tS, sr);
-        const bool diag = CAUSAL && i == j;
         const int qlo = 64 * wg;
+        // query columns below thr are masked for this key row
+        int thr = r;
+        bool diag = CAUSAL && i == j;
+        if constexpr (VAR) {
+          thr = key_thr - i * kTile;
+          diag = thr > qlo;
+        }
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -529,9 +723,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  make_float2(sl2, sl2), make_float2(-l2.x, -l2.y));
           float p0 = ex2_approx(x.x);
           float p1 = ex2_approx(x.y);
-          if (diag) {  // query q sees key r only if r <= q
-            p0 = (qlo + 2 * c < r) ? 0.f : p0;
-            p1 = (qlo + 2 * c + 1 < r) ? 0.f : p1;
+          if (diag) {  // query q sees key r only if r <= q (+ nk - nq)
+            p0 = (qlo + 2 * c < thr) ? 0.f : p0;
+            p1 = (qlo + 2 * c + 1 < thr) ? 0.f : p1;
           }
           pk[c] = pack_bf16x2(p0, p1);
         }
@@ -581,9 +775,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int key = j * kTile + r;
-      const bool store = key < a.N;
-      __nv_bfloat16* out = wg == 0 ? a.dv + row_offset(a.sdv, bh, a.H, key)
-                                   : a.dk + row_offset(a.sdk, bh, a.H, key);
+      bool store;
+      __nv_bfloat16* out;
+      if constexpr (VAR) {
+        const Seq sq = seq_of(bh, a.g);
+        store = key < sq.nk;
+        const Strides& so = wg == 0 ? a.sdv : a.sdk;
+        out = (wg == 0 ? a.dv : a.dk) + sq.bb * so.batch + sq.hh * so.head +
+              static_cast<int64_t>(sq.k0 + key) * so.row;
+      } else {
+        store = key < a.N;
+        out = wg == 0 ? a.dv + row_offset(a.sdv, bh, a.H, key)
+                      : a.dk + row_offset(a.sdk, bh, a.H, key);
+      }
       const float mul = wg == 0 ? 1.f : a.scale;
       const uint32_t col = wg == 0 ? kColDV : Cfg::col_dk();
 #pragma unroll 1
@@ -619,9 +823,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (item >= a.n_items) break;  // only in the last, partial round
         int bh, j;
         decode_kv_item(item, a, CAUSAL, bh, j);
-        const int n_it = CAUSAL ? n_q - j : n_q;
+        int n_it, nq_rows;
+        KvWork w;
+        float* acc_base;  // accumulator row 0 of this (sequence, head)
+        if constexpr (VAR) {
+          const Seq sq = seq_of(bh, a.g);
+          w = var_kv_work(j, sq, CAUSAL);
+          n_it = w.n_it;
+          nq_rows = sq.nq;
+          acc_base = a.ws + 2 * static_cast<size_t>(a.planes) * a.lpad +
+                     ((static_cast<size_t>(sq.bb) * a.g.H + sq.hh) * a.g.rows_q + sq.q0) * D;
+        } else {
+          n_it = CAUSAL ? n_q - j : n_q;
+          nq_rows = a.N;
+          acc_base = a.ws.dq_acc(a.BH, a.Npad) + static_cast<size_t>(bh) * a.N * D;
+        }
         for (int u = 0; u < n_it; ++u, ++it) {
-          const int i = qblock_at(j, u, n_q, CAUSAL);
+          int i;
+          if constexpr (VAR)
+            i = var_qblock(w, u, CAUSAL);
+          else
+            i = qblock_at(j, u, n_q, CAUSAL);
           ok = mbar_wait_warp(smem_u32(&bars->dq_full), it & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
@@ -630,8 +852,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // All 128 columns go to registers first and TMEM is released
             // before any atomic is issued, so the next dP^T never waits on them.
             const int dd = wq * 32 + lane;
-            const int rows = min(kTile, a.N - i * kTile);
-            float* dst = a.ws.dq_acc(a.BH, a.Npad) + (static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile) * D + dd;
+            const int rows = min(kTile, nq_rows - i * kTile);
+            float* dst = acc_base + static_cast<size_t>(i) * kTile * D + dd;
             uint32_t v[64], w[64];
             tmem_ld64(t_lane + kColDP, v);
             tmem_ld64(t_lane + kColDP + 64, w);
@@ -661,8 +883,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
             const int row = i * kTile + wq * 32 + lane;
-            if (row < a.N) {
-              float4* dst = reinterpret_cast<float4*>(a.ws.dq_acc(a.BH, a.Npad) + (static_cast<size_t>(bh) * a.N + row) * D);
+            if (row < nq_rows) {
+              float4* dst = reinterpret_cast<float4*>(acc_base + static_cast<size_t>(row) * D);
 #pragma unroll
               for (int c = 0; c < D / 4; ++c)
                 atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
@@ -693,7 +915,7 @@ cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const PreArg
   }
   if (stages & kStageDkdv) {
     constexpr int smem = bwd_smem_bytes<D>();
-    auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+    auto kern = bwd_dkdv_kernel<D, CAUSAL, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int grid = min(a.n_items, p.num_sms);
@@ -710,7 +932,106 @@ cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const PreArg
   return cudaSuccess;
 }
 
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_var_t(const Problem& p, const CUtensorMap* maps, const PreVarArgs& pa,
+                             const BwdVarArgs& a, const DqArgs& qa, cudaStream_t stream) {
+  {
+    const size_t work = static_cast<size_t>(pa.BH) * pa.max_q_pad * (D <= 32 ? 4 : (D <= 64 ? 8 : 16));
+    const int grid = static_cast<int>(std::min<size_t>((work + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
+    bwd_pre_var_kernel<D><<<grid, 256, 0, stream>>>(pa);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    constexpr int smem = bwd_smem_bytes<D>();
+    auto kern = bwd_dkdv_kernel<D, CAUSAL, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = min(a.n_items, p.num_sms);
+    kern<<<grid, kBwdThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const size_t n8 = static_cast<size_t>(qa.BH) * qa.N * D / 8;
+  const int grid = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
+  dq_convert_kernel<D><<<grid, 256, 0, stream>>>(qa, n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_var(const Problem& p, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                           void* dv, void* workspace, cudaStream_t stream) {
+  const bool packed = p.cu_q != nullptr;
+  const int planes_b = packed ? 1 : p.B;
+  CUtensorMap maps[4];
+  if (!make_tile_map(&maps[0], q, planes_b, p.H, p.rows_q, p.d, p.st[kQ]) ||
+      !make_tile_map(&maps[1], k, planes_b, p.H, p.rows_k, p.d, p.st[kK]) ||
+      !make_tile_map(&maps[2], v, planes_b, p.H, p.rows_k, p.d, p.st[kV]) ||
+      !make_tile_map(&maps[3], dO, planes_b, p.H, p.rows_q, p.d, p.st[kdO]))
+    return cudaErrorInvalidValue;
+  const VarGeom g{p.cu_q, p.cu_k, p.H, p.N, p.Nk, p.rows_q, p.rows_k, p.max_q, p.max_k};
+  const int planes = planes_b * p.H;
+  const int lpad = var_padded_rows(packed, p.B, p.rows_q);
+  float* ws = static_cast<float*>(workspace);
+  PreVarArgs pa;
+  pa.o = static_cast<const __nv_bfloat16*>(o);
+  pa.dO = static_cast<const __nv_bfloat16*>(dO);
+  pa.lse = lse;
+  pa.ws = ws;
+  pa.so = p.st[kO];
+  pa.sdo = p.st[kdO];
+  pa.planes = planes;
+  pa.lpad = lpad;
+  pa.max_q_pad = (p.max_q + kTile - 1) / kTile * kTile;
+  pa.BH = p.B * p.H;
+  pa.g = g;
+  BwdVarArgs a;
+  a.ws = ws;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.status = p.status;
+  a.BH = p.B * p.H;
+  a.n_tiles = (p.max_k + kTile - 1) / kTile;
+  a.n_items = a.BH * a.n_tiles;
+  a.planes = planes;
+  a.lpad = lpad;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.sdk = p.st[kdK];
+  a.sdv = p.st[kdV];
+  a.g = g;
+  DqArgs qa;  // the accumulator as planes x rows_q rows after 2 x planes x lpad floats
+  qa.ws = Workspace{ws};
+  qa.dq = static_cast<__nv_bfloat16*>(dq);
+  qa.sdq = p.st[kdQ];
+  qa.N = p.rows_q;
+  qa.H = p.H;
+  qa.Npad = lpad;
+  qa.BH = planes;
+  qa.scale = p.scale;
+  switch (p.d) {
+    case 32:
+      return p.causal ? launch_bwd_var_t<32, true>(p, maps, pa, a, qa, stream)
+                      : launch_bwd_var_t<32, false>(p, maps, pa, a, qa, stream);
+    case 64:
+      return p.causal ? launch_bwd_var_t<64, true>(p, maps, pa, a, qa, stream)
+                      : launch_bwd_var_t<64, false>(p, maps, pa, a, qa, stream);
+    case 96:
+      return p.causal ? launch_bwd_var_t<96, true>(p, maps, pa, a, qa, stream)
+                      : launch_bwd_var_t<96, false>(p, maps, pa, a, qa, stream);
+    default:
+      return p.causal ? launch_bwd_var_t<128, true>(p, maps, pa, a, qa, stream)
+                      : launch_bwd_var_t<128, false>(p, maps, pa, a, qa, stream);
+  }
+}
+
 }  // namespace
+
+size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int d) {
+  const size_t planes = static_cast<size_t>(packed ? 1 : B) * H;
+  const size_t lpad = static_cast<size_t>(var_padded_rows(packed, B, rows_q));
+  return (2 * planes * lpad + planes * static_cast<size_t>(rows_q) * d) * 4;
+}
 
 size_t bwd_workspace_bytes(int B, int H, int N, int d) {
   const size_t BH = static_cast<size_t>(B) * H;
@@ -721,6 +1042,10 @@ size_t bwd_workspace_bytes(int B, int H, int N, int d) {
 cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const void* v,
                        const void* o, const float* lse, const void* dO, void* dq, void* dk,
                        void* dv, void* workspace, int stages, cudaStream_t stream) {
+  if (p.var) {
+    if (stages != kStagesAll) return cudaErrorInvalidValue;
+    return launch_bwd_var(p, q, k, v, o, lse, dO, dq, dk, dv, workspace, stream);
+  }
   const int BH = p.B * p.H;
   CUtensorMap maps[4];
   if ((stages & kStageDkdv) && (!make_tile_map(&maps[0], q, p.B, p.H, p.N, p.d, p.st[kQ]) ||

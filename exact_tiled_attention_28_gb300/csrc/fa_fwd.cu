@@ -35,6 +35,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "schedule.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -98,7 +99,29 @@ struct FwdArgs {
   Strides so;  // element strides of o
 };
 
-__device__ __forceinline__ void decode_item(int item, const FwdArgs& a, bool causal, int& bh,
+// Arguments of the kernel for sequences of unequal lengths (dense or packed
+// batch); sh = b * H + h runs over sequences and heads.
+struct FwdVarArgs {
+  __nv_bfloat16* o;
+  float* lse;  // [planes, rows_q] with planes = batch coordinates x H
+  int* status;
+  int BH, n_pairs, n_items;  // BH = sequences x heads; pairs of the longest sequence
+  float scale, scale_log2;
+  Strides so;
+  VarGeom g;
+};
+
+template <bool VAR>
+struct FwdArgsOf {
+  using type = FwdArgs;
+};
+template <>
+struct FwdArgsOf<true> {
+  using type = FwdVarArgs;
+};
+
+template <class Args>
+__device__ __forceinline__ void decode_item(int item, const Args& a, bool causal, int& bh,
                                             int& pair) {
   if (causal) {  // longest first: the last query pairs of every head come first
     pair = a.n_pairs - 1 - item / a.BH;
@@ -115,10 +138,24 @@ __device__ __forceinline__ int tile_steps(int qt, const FwdArgs& a, bool causal)
   return causal ? min(qt + 1, a.n_tiles) : a.n_tiles;
 }
 
-template <int D, bool CAUSAL>
+// The same for a sequence of unequal lengths. A tile whose rows see no key
+// at all (causal with nq > nk, or nk = 0) still runs one fully masked step,
+// which leaves l = 0: its rows get O = 0 and LSE = -inf.
+__device__ __forceinline__ int var_tile_steps(int qt, const Seq& s, bool causal) {
+  if (qt * kTile >= s.nq) return 0;
+  const int nkt = (s.nk + kTile - 1) / kTile;
+  int n = nkt;
+  if (causal) {
+    const int last_key = min(qt * kTile + kTile - 1, s.nq - 1) + s.nk - s.nq;
+    n = last_key < 0 ? 0 : min(nkt, last_key / kTile + 1);
+  }
+  return max(n, 1);
+}
+
+template <int D, bool CAUSAL, bool VAR>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+               const __grid_constant__ CUtensorMap tmV, const typename FwdArgsOf<VAR>::type a) {
   using Cfg = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -173,8 +210,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (item >= a.n_items) break;  // only in the last, partial round
         int bh, pair;
         decode_item(item, a, CAUSAL, bh, pair);
-        const int hh = bh % a.H, bb = bh / a.H;
-        const int J = max(tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL));
+        int hh, bb, q0 = 0, k0 = 0, J;
+        if constexpr (VAR) {
+          const Seq sq = seq_of(bh, a.g);
+          hh = sq.hh;
+          bb = sq.bb;
+          q0 = sq.q0;
+          k0 = sq.k0;
+          J = max(var_tile_steps(2 * pair, sq, CAUSAL), var_tile_steps(2 * pair + 1, sq, CAUSAL));
+          if (J == 0) continue;  // every tile of the pair lies past the sequence
+        } else {
+          hh = bh % a.H;
+          bb = bh / a.H;
+          J = max(tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL));
+        }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -184,7 +233,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
           for (int cb = 0; cb < Cfg::kColBlocks; ++cb)
             tma_load_4d(sQ + (t * Cfg::kColBlocks + cb) * kBlockBytes, &tmQ, bar, 64 * cb,
-                        (2 * pair + t) * kTile, hh, bb, pol_q);
+                        q0 + (2 * pair + t) * kTile, hh, bb, pol_q);
           ++q_issued[t];
         }
         for (int j = 0; j < J && ok; ++j) {
@@ -197,7 +246,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
             for (int cb = 0; cb < Cfg::kColBlocks; ++cb)
               tma_load_4d(sKV + (s * Cfg::kColBlocks + cb) * kBlockBytes, w ? &tmV : &tmK, bar,
-                          64 * cb, j * kTile, hh, bb, pol_kv);
+                          64 * cb, k0 + j * kTile, hh, bb, pol_kv);
             ++kv_it;
           }
         }
@@ -257,7 +306,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (item >= a.n_items) break;  // only in the last, partial round
         int bh, pair;
         decode_item(item, a, CAUSAL, bh, pair);
-        const int Jt[2] = {tile_steps(2 * pair, a, CAUSAL), tile_steps(2 * pair + 1, a, CAUSAL)};
+        int Jt[2];
+        if constexpr (VAR) {
+          const Seq sq = seq_of(bh, a.g);
+          Jt[0] = var_tile_steps(2 * pair, sq, CAUSAL);
+          Jt[1] = var_tile_steps(2 * pair + 1, sq, CAUSAL);
+          if (Jt[0] == 0 && Jt[1] == 0) {  // skipped by the loader too: no Q round
+            --q_round;
+            continue;
+          }
+        } else {
+          Jt[0] = tile_steps(2 * pair, a, CAUSAL);
+          Jt[1] = tile_steps(2 * pair + 1, a, CAUSAL);
+        }
         const int J = max(Jt[0], Jt[1]);
         const uint32_t base = kv_it;
 #pragma unroll
@@ -343,7 +404,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int bh, pair;
       decode_item(item, a, CAUSAL, bh, pair);
       const int qt = 2 * pair + t;
-      const int J = tile_steps(qt, a, CAUSAL);
+      int J;
+      int key_lim = 0;  // VAR: the last key this row may see, relative to the sequence
+      if constexpr (VAR) {
+        const Seq sq = seq_of(bh, a.g);
+        J = var_tile_steps(qt, sq, CAUSAL);
+        key_lim = sq.nk - 1;
+        if (CAUSAL) key_lim = min(key_lim, qt * kTile + r + sq.nk - sq.nq);
+      } else {
+        J = tile_steps(qt, a, CAUSAL);
+      }
       if (J == 0) continue;
       float m = NEG_INF, l = 0.f;
       for (int j = 0; j < J; ++j) {
@@ -357,8 +427,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
         // masks: causal diagonal tile, and keys past N in the last tile
         int lim = 127;
-        if (CAUSAL && j == qt) lim = r;
-        if (j == a.n_tiles - 1) lim = min(lim, a.N - 1 - j * kTile);
+        if constexpr (VAR) {  // keys past the row's causal limit or past the sequence
+          lim = min(lim, key_lim - j * kTile);
+        } else {
+          if (CAUSAL && j == qt) lim = r;
+          if (j == a.n_tiles - 1) lim = min(lim, a.N - 1 - j * kTile);
+        }
         const bool masked = lim < 127;
         if (masked) {
 #pragma unroll
@@ -439,10 +513,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int row = qt * kTile + r;
-      const bool store = row < a.N;
-      const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = a.o + (bh / a.H) * a.so.batch + (bh % a.H) * a.so.head +
-                            static_cast<int64_t>(row) * a.so.row;
+      bool store;
+      float inv_l;
+      __nv_bfloat16* orow;
+      Seq sq;
+      if constexpr (VAR) {  // a row that saw no key has l = 0: O = 0, LSE = -inf
+        sq = seq_of(bh, a.g);
+        store = row < sq.nq;
+        inv_l = l > 0.f ? 1.f / l : 0.f;
+        orow = a.o + sq.bb * a.so.batch + sq.hh * a.so.head +
+               static_cast<int64_t>(sq.q0 + row) * a.so.row;
+      } else {
+        store = row < a.N;
+        inv_l = 1.f / l;
+        orow = a.o + (bh / a.H) * a.so.batch + (bh % a.H) * a.so.head +
+               static_cast<int64_t>(row) * a.so.row;
+      }
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -460,9 +546,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      if (store)
-        a.lse[static_cast<size_t>(bh) * a.N + row] =
-            fmaf(m, a.scale, lg2_approx(l) * 0.69314718055994531f);
+      if constexpr (VAR) {
+        if (store)
+          a.lse[static_cast<size_t>(sq.bb * a.g.H + sq.hh) * a.g.rows_q + sq.q0 + row] =
+              l > 0.f ? fmaf(m, a.scale, lg2_approx(l) * 0.69314718055994531f)
+                      : __int_as_float(0xff800000);
+      } else {
+        if (store)
+          a.lse[static_cast<size_t>(bh) * a.N + row] =
+              fmaf(m, a.scale, lg2_approx(l) * 0.69314718055994531f);
+      }
     }
   }
 
@@ -472,11 +565,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VAR = false>
 cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                         const CUtensorMap& mv, const FwdArgs& a, cudaStream_t stream) {
+                         const CUtensorMap& mv, const typename FwdArgsOf<VAR>::type& a,
+                         cudaStream_t stream) {
   constexpr int smem = fwd_smem_bytes<D>();
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, CAUSAL, VAR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = min(a.n_items, p.num_sms);
@@ -486,8 +580,45 @@ cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensor
 
 }  // namespace
 
+cudaError_t launch_fwd_var(const Problem& p, const void* q, const void* k, const void* v,
+                           void* o, float* lse, cudaStream_t stream) {
+  const bool packed = p.cu_q != nullptr;
+  const int planes_b = packed ? 1 : p.B;
+  CUtensorMap mq, mk, mv;
+  if (!make_tile_map(&mq, q, planes_b, p.H, p.rows_q, p.d, p.st[kQ]) ||
+      !make_tile_map(&mk, k, planes_b, p.H, p.rows_k, p.d, p.st[kK]) ||
+      !make_tile_map(&mv, v, planes_b, p.H, p.rows_k, p.d, p.st[kV]))
+    return cudaErrorInvalidValue;
+  FwdVarArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = p.status;
+  a.BH = p.B * p.H;
+  a.n_pairs = ((p.max_q + kTile - 1) / kTile + 1) / 2;
+  a.n_items = a.BH * a.n_pairs;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.so = p.st[kO];
+  a.g = VarGeom{p.cu_q, p.cu_k, p.H, p.N, p.Nk, p.rows_q, p.rows_k, p.max_q, p.max_k};
+  switch (p.d) {
+    case 32:
+      return p.causal ? launch_fwd_t<32, true, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<32, false, true>(p, mq, mk, mv, a, stream);
+    case 64:
+      return p.causal ? launch_fwd_t<64, true, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<64, false, true>(p, mq, mk, mv, a, stream);
+    case 96:
+      return p.causal ? launch_fwd_t<96, true, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<96, false, true>(p, mq, mk, mv, a, stream);
+    default:
+      return p.causal ? launch_fwd_t<128, true, true>(p, mq, mk, mv, a, stream)
+                      : launch_fwd_t<128, false, true>(p, mq, mk, mv, a, stream);
+  }
+}
+
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream) {
+  if (p.var) return launch_fwd_var(p, q, k, v, o, lse, stream);
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
   if (!make_tile_map(&mq, q, p.B, p.H, p.N, p.d, p.st[kQ]) ||

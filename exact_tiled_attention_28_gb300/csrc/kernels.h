@@ -28,6 +28,17 @@ struct Problem {
   int num_sms;
   int* status;  // device address of the status word
   Strides st[kNumTensors];
+  // Sequences of unequal query and key lengths (var = 1), causal mask aligned
+  // at the bottom right. Dense batch (cu_q null): B sequences of N query and
+  // Nk key rows in [B, H, N | Nk, d] tensors. Packed batch: sequence b owns
+  // rows cu_q[b]..cu_q[b+1]-1 of q and cu_k[b]..cu_k[b+1]-1 of k and v,
+  // which hold rows_q and rows_k rows per head (batch coordinate 0); max_q
+  // and max_k bound the lengths.
+  int var;
+  int Nk;
+  const int* cu_q;
+  const int* cu_k;
+  int rows_q, rows_k, max_q, max_k;
 };
 
 // Contiguous [B, H, N, d] strides.
@@ -52,5 +63,17 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
                        void* dv, void* workspace, int stages, cudaStream_t stream);
 
 size_t bwd_workspace_bytes(int B, int H, int N, int d);
+
+// Workspace of the backward for unequal lengths (packed = false: B dense
+// sequences of rows_q query rows) or a packed batch of B sequences with
+// rows_q query rows in all: D and the log2 LSE rows (fp32) padded per
+// sequence, then the fp32 dQ accumulator.
+size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int d);
+
+// Records DEV_BADARG in the status word when the packed batch's offsets are
+// not non-decreasing from 0 to rows_q / rows_k or a length exceeds max_q /
+// max_k. The kernels clamp every offset, so such offsets give wrong results
+// but no access outside the buffers.
+cudaError_t launch_varlen_check(const Problem& p, cudaStream_t stream);
 
 }  // namespace fa

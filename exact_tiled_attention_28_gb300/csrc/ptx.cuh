@@ -15,6 +15,7 @@ namespace fa {
 enum DeviceStatus : int {
   DEV_OK = 0,
   DEV_TIMEOUT = 1,  // a bounded barrier wait ran out
+  DEV_BADARG = 2,   // a packed batch's sequence offsets are malformed
 };
 
 // Wall-clock limit of one barrier wait. No wait in these kernels legitimately

@@ -74,6 +74,36 @@ def attention_inputs(seed: int, B: int, H: int, N: int, d: int,
     return {t: tensor_bits(seed, t, B, H, N, d) for t in tensors}
 
 
+# Inputs of unequal lengths: q and dO of (sequence b, head h) come from
+# ``seed``, k and v from ``seed + KV_SEED_OFFSET``, each block drawn for its own
+# length.
+KV_SEED_OFFSET = 500
+
+
+def nqnk_inputs(seed: int, B: int, H: int, Nq: int, Nk: int, d: int) -> dict:
+    """Dict name -> bf16 bits: q, do [B, H, Nq, d] and k, v [B, H, Nk, d]."""
+    out = attention_inputs(seed, B, H, Nq, d, ("q", "do"))
+    out.update(attention_inputs(seed + KV_SEED_OFFSET, B, H, Nk, d, ("k", "v")))
+    return out
+
+
+def packed_inputs(seed: int, lens_q, lens_k, H: int, d: int):
+    """A packed batch: (dict name -> bf16 bits [T, H, d] with q, do on
+    sum(lens_q) rows and k, v on sum(lens_k) rows, cu_q, cu_k int32 prefix
+    offsets). Block (b, h) of each tensor is the head generator's [n, d] draw."""
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    out = {n: np.zeros((int(cu[-1]), H, d), dtype=np.uint16)
+           for n, cu in (("q", cu_q), ("do", cu_q), ("k", cu_k), ("v", cu_k))}
+    for b, (nq, nk) in enumerate(zip(lens_q, lens_k)):
+        for h in range(H):
+            for n, s, cu, length in (("q", seed, cu_q, nq), ("do", seed, cu_q, nq),
+                                     ("k", seed + KV_SEED_OFFSET, cu_k, nk),
+                                     ("v", seed + KV_SEED_OFFSET, cu_k, nk)):
+                out[n][cu[b]:cu[b + 1], h] = head_bits(s, n, b, h, int(length), d)
+    return out, cu_q, cu_k
+
+
 def head_inputs_f64(seed: int, b: int, h: int, N: int, d: int,
                     tensors=("q", "k", "v", "do")) -> dict:
     """Dict tensor name -> float64 [N, d] for one head (exact bf16 values)."""

@@ -136,6 +136,59 @@ fa_status fa_bwd_dq_finalize(void* dq, int B, int H, int N, int d, float scale, 
                              size_t workspace_bytes, void* stream);
 
 /*
+ * Sequences of unequal lengths. The pages state the method for one length N;
+ * for serving batches of requests of different lengths ("Flash Attention v2"
+ * notes, "Performance Comparison: v1 vs v2", continuous batching; "Detailed
+ * Differences", 4 "Batch and Sequence Length Support") they fix no
+ * convention. Here Nq query rows attend to Nk key rows and the causal mask
+ * is aligned at the bottom right: query i sees key j when j <= i + Nk - Nq,
+ * so the last query sees every key; with Nq = Nk this is the rule above. A
+ * query row that sees no key (causal with Nq > Nk, or a sequence with no
+ * keys) gets o = 0 and lse = -inf, and its gradients are zero.
+ *
+ * fa_fwd_nqnk / fa_bwd_nqnk: B dense sequences, q, o, dO, dq of shape
+ * [B, H, Nq, d] and k, v, dk, dv of shape [B, H, Nk, d] (Nq, Nk >= 1); lse is
+ * fp32 [B, H, Nq]. strides: as for fa_fwd_strided / fa_bwd_strided (12 or
+ * 24), or NULL for contiguous tensors. fa_bwd_nqnk takes a workspace of
+ * fa_bwd_workspace_size(B, H, Nq, d) bytes. Errors as for fa_fwd / fa_bwd.
+ */
+fa_status fa_fwd_nqnk(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, const long long* strides, int causal,
+                      float scale, void* stream);
+fa_status fa_bwd_nqnk(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                      int H, int Nq, int Nk, int d, const long long* strides, int causal,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_fwd_varlen / fa_bwd_varlen: a packed batch of B sequences along the
+ * token axis. q, o, dO, dq hold total_q rows and k, v, dk, dv total_k rows,
+ * each row H heads of d values: [total, H, d] when strides is NULL, else
+ * strides gives (head, row) element strides per tensor (8 numbers for q, k,
+ * v, o; 16 for q, k, v, o, dO, dq, dk, dv), positive multiples of 8.
+ * cu_seqlens_q, cu_seqlens_k: DEVICE int32 arrays of B + 1 prefix offsets
+ * (0 = cu[0] <= cu[1] <= ... <= cu[B] = total); sequence b owns query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1]-1, and may be empty. max_seqlen_q / max_seqlen_k (>= 1)
+ * bound the lengths. lse is fp32 [H, total_q]. The offsets are read on the
+ * device: offsets that break these rules give wrong results but no access
+ * outside the buffers, and are reported as FA_ERR_INVALID_ARG by the next
+ * fa_last_device_status(). fa_bwd_varlen takes a workspace of
+ * fa_bwd_varlen_workspace_size(B, H, total_q, d) bytes.
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                        const long long* strides, int causal, float scale, void* stream);
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int d);
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                        const long long* strides, int causal, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
  * Self-test of the failure path (no counterpart in the method): enqueues a
  * one-thread kernel that waits on an on-chip barrier nothing ever arrives on,
  * with a limit of limit_ms milliseconds (1..2000) instead of the 2 s the
@@ -183,8 +236,10 @@ const char* fa_status_string(int status);
 
 /*
  * Synchronises the stream, then returns FA_ERR_TIMEOUT if any kernel of this
- * process has recorded a bounded-wait timeout since the last call (and clears
- * the record), FA_ERR_CUDA if the synchronisation failed, else FA_OK.
+ * process has recorded a bounded-wait timeout since the last call,
+ * FA_ERR_INVALID_ARG if a packed batch's offsets broke the rules of
+ * fa_fwd_varlen (the first such record wins; the call clears it),
+ * FA_ERR_CUDA if the synchronisation failed, else FA_OK.
  */
 fa_status fa_last_device_status(void* stream);
 

@@ -142,3 +142,44 @@ def test_strided_entry_points_reject_bad_strides(lib):
         fa.FA_ERR_INVALID_ARG
     assert lib.fa_bwd_strided(*([P] * 9), 1, 4, 8, 64, None, 0, 0.125, P, 1 << 20, None) == \
         fa.FA_ERR_INVALID_ARG
+
+
+def test_nqnk_entry_points_reject_before_launch(lib):
+    def fwd(q=P, B=1, H=2, Nq=100, Nk=300, d=64, st=None, scale=0.125):
+        return lib.fa_fwd_nqnk(q, P, P, P, P, B, H, Nq, Nk, d, st, 1, scale, None)
+
+    assert fwd(q=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd(Nk=0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(Nq=0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    bad = (ctypes.c_longlong * 12)(*([64 * 300 * 2, 64 * 300, 64] * 3 + [64, 0, 64]))
+    assert fwd(st=bad) == fa.FA_ERR_INVALID_ARG
+    ws_ok = fa.fa_bwd_workspace_size(1, 2, 100, 64)
+    assert lib.fa_bwd_nqnk(*([P] * 9), 1, 2, 100, 300, 64, None, 1, 0.125, P, ws_ok - 1,
+                           None) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd_nqnk(*([P] * 8), None, 1, 2, 100, 300, 64, None, 1, 0.125, P, ws_ok,
+                           None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_varlen_entry_points_reject_before_launch(lib):
+    def fwd(cu_q=P, cu_k=P, B=3, H=2, Tq=500, Tk=700, mq=300, mk=400, d=128, st=None):
+        return lib.fa_fwd_varlen(P, P, P, P, P, cu_q, cu_k, B, H, Tq, Tk, mq, mk, d, st, 1,
+                                 0.1, None)
+
+    assert fwd(cu_q=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd(cu_k=P + 2) == fa.FA_ERR_INVALID_ARG
+    for kw in (dict(Tk=0), dict(mq=0), dict(mk=0), dict(B=0), dict(Tq=0)):
+        assert fwd(**kw) == fa.FA_ERR_INVALID_ARG, kw
+    assert fwd(d=256) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(B=1 << 20, H=1 << 11, mq=1 << 10) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(st=(ctypes.c_longlong * 8)(128, 256, 128, 256, 128, 256, 128, 12)) == \
+        fa.FA_ERR_INVALID_ARG
+    ws = fa.fa_bwd_varlen_workspace_size(3, 2, 500, 128)
+    # D and lse2 padded per sequence, plus the fp32 accumulator
+    assert ws >= 4 * (2 * 2 * (512 + 128 * 4) + 2 * 500 * 128)
+    assert fa.fa_bwd_varlen_workspace_size(3, 2, 500, 48) == 0
+    assert lib.fa_bwd_varlen(*([P] * 11), 3, 2, 500, 700, 300, 400, 128, None, 0, 0.1, P, ws - 1,
+                             None) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd_varlen(*([P] * 11), 3, 2, 500, 700, 300, 400, 128, None, 0, 0.1, None, ws,
+                             None) == fa.FA_ERR_WORKSPACE
