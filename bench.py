@@ -45,6 +45,18 @@ WORKLOADS["dim_d32_n4096"] = (4, 64, 4096, 32)
 WORKLOADS["dim_d96_n4096"] = (4, 16, 4096, 96)
 DEFAULT_WORKLOAD = "gpt_d128_n4096"
 
+# Packed batches of variable-length sequences (fa_fwd_varlen / fa_bwd_varlen):
+# name -> (sequences, H, d, shortest, longest, length seed); the lengths are
+# drawn uniformly from [shortest, longest] with the seed, equal for q and k.
+VARLEN_WORKLOADS = {"varlen_d128_s16_256to4096": (16, 16, 128, 256, 4096, 7),
+                    "varlen_d64_s64_64to1024": (64, 32, 64, 64, 1024, 8)}
+
+
+def varlen_lengths(name):
+    import numpy as np
+    S, _, _, lo, hi, seed = VARLEN_WORKLOADS[name]
+    return [int(n) for n in np.random.default_rng(seed).integers(lo, hi + 1, size=S)]
+
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dK/dV kernel,
 # from an ncu capture of the current kernel source (see profiles/), keyed by
 # workload and causal flag; None where no capture of the current kernel exists.
@@ -126,22 +138,29 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the fp64 oracle on the host cores (bounded sample)
 
-def oracle_sample(B, H, N, d, causal, seed, budget_s, max_heads):
+def oracle_sample(B, H, N, d, causal, seed, budget_s, max_heads, lengths=None):
     """Times oracle forward + backward on whole heads of the workload until
-    budget_s has passed (at least one head). Returns (TFLOP/s, heads, seconds)."""
+    budget_s has passed (at least one head). With ``lengths`` (a packed batch)
+    head b*H + h is sequence b's head h. Returns (TFLOP/s, heads, seconds)."""
     import oracle
     from exact_tiled_attention_28_gb300 import inputs
     scale = 1.0 / math.sqrt(d)
-    heads, spent = 0, 0.0
+    heads, spent, flops = 0, 0.0, 0.0
+    nseq = B if lengths is None else len(lengths)
     while heads < max_heads and (heads == 0 or spent < budget_s):
-        b, h = divmod(heads % (B * H), H)
-        x = inputs.head_inputs_f64(seed, b, h, N, d)
+        b, h = divmod(heads % (nseq * H), H)
+        n = N if lengths is None else lengths[b]
+        if lengths is None:
+            x = inputs.head_inputs_f64(seed, b, h, n, d)
+        else:  # the packed generator's block (b, h)
+            x = inputs.head_inputs_f64(seed, b, h, n, d, ("q", "do"))
+            x.update(inputs.head_inputs_f64(seed + inputs.KV_SEED_OFFSET, b, h, n, d, ("k", "v")))
         t0 = time.perf_counter()
         oracle.head_forward(x["q"], x["k"], x["v"], causal, scale)
         oracle.head_backward(x["q"], x["k"], x["v"], x["do"], causal, scale)
         spent += time.perf_counter() - t0
+        flops += 3.5 * fwd_flops(1, 1, n, d, causal)
         heads += 1
-    flops = 3.5 * fwd_flops(1, 1, N, d, causal) * heads
     return flops / spent / 1e12, heads, spent
 
 
@@ -157,7 +176,8 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS))
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--layout", default="bhnd", choices=("bhnd", "bnhd"),
                     help="memory layout of q, k, v, o, dO and the gradients")
@@ -189,32 +209,41 @@ def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
-    B, H, N, d = WORKLOADS[args.workload]
+    lengths = None
+    if args.workload in VARLEN_WORKLOADS:
+        S, H, d = VARLEN_WORKLOADS[args.workload][:3]
+        lengths = varlen_lengths(args.workload)
+        B, N = S, max(lengths)
+    else:
+        B, H, N, d = WORKLOADS[args.workload]
     for _ in range(args.warmup):
-        oracle_sample(B, H, N, d, args.causal, 1000, 0.0, 1)
+        oracle_sample(B, H, N, d, args.causal, 1000, 0.0, 1, lengths)
     t0 = time.perf_counter()
     flops = 0.0
-    for _ in range(args.steps):
-        oracle_sample(B, H, N, d, args.causal, 1000, 0.0, 1)
-        flops += 3.5 * fwd_flops(1, 1, N, d, args.causal)
+    for _ in range(args.steps):  # each step: the first head of the workload, fwd + bwd
+        tf, _, spent = oracle_sample(B, H, N, d, args.causal, 1000, 0.0, 1, lengths)
+        flops += tf * 1e12 * spent
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(args, B, H, N, d),
+            "config": (config_of(args, B, H, N, d) if lengths is None
+                       else varlen_config_of(args, lengths, H, d)),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
                              "kind": "oracle",
-                             "sample": f"one head (N={N}, d={d}) fwd+bwd per step"},
+                             "sample": f"one head (first sequence, d={d}) fwd+bwd per step"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, steps):
+def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, steps,
+            compute=None):
     """Times `steps` end-to-end steps (H2D of the inputs, fa_fwd + fa_bwd, D2H of
-    every output) with the three stages pipelined across steps. Returns
+    every output) with the three stages pipelined across steps. ``compute(xb,
+    ob, wb, stream)`` replaces the fa_fwd + fa_bwd pair when given. Returns
     (ms per step, H2D bytes, D2H bytes, H2D GB/s alone, D2H GB/s alone)."""
     outs0 = {"o": o0, "lse": lse0, "dq": dq0, "dk": dk0, "dv": dv0}
     bufs = [({n: t for n, t in x0.items()}, outs0, ws0),
@@ -244,9 +273,12 @@ def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, st
         s_comp.wait_event(in_done[k])
         if k >= 2:
             s_comp.wait_event(out_done[k - 2])  # outputs k % 2 copied out
-        fa.fa_fwd(xb["q"], xb["k"], xb["v"], ob["o"], ob["lse"], causal, scale, stream=s_comp)
-        fa.fa_bwd(xb["q"], xb["k"], xb["v"], ob["o"], ob["lse"], xb["do"], ob["dq"], ob["dk"],
-                  ob["dv"], causal, scale, wb, stream=s_comp)
+        if compute is not None:
+            compute(xb, ob, wb, s_comp)
+        else:
+            fa.fa_fwd(xb["q"], xb["k"], xb["v"], ob["o"], ob["lse"], causal, scale, stream=s_comp)
+            fa.fa_bwd(xb["q"], xb["k"], xb["v"], ob["o"], ob["lse"], xb["do"], ob["dq"], ob["dk"],
+                      ob["dv"], causal, scale, wb, stream=s_comp)
         comp_done[k].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[k])
@@ -270,6 +302,150 @@ def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, st
     h2d_gbs = bw(lambda: [bufs[0][0][n].copy_(host[n], non_blocking=True) for n in host], h2d)
     d2h_gbs = bw(lambda: [out_host[0][n].copy_(t, non_blocking=True) for n, t in outs0.items()], d2h)
     return ms, h2d, d2h, h2d_gbs, d2h_gbs
+
+
+def varlen_config_of(args, lengths, H, d):
+    T = sum(lengths)
+    return {"workload": f"{args.workload}: {len(lengths)} packed sequences of "
+                        f"{min(lengths)}..{max(lengths)} tokens (T={T}), H={H} d={d} "
+                        f"{'causal' if args.causal else 'non-causal'} fwd+bwd",
+            "sequences": len(lengths), "total_tokens": T, "max_seqlen": max(lengths),
+            "H": H, "d": d, "causal": bool(args.causal), "scale": "1/sqrt(d)",
+            "global_batch": len(lengths) * args.gpus, "seq_len": max(lengths),
+            "parallelism": f"replicas x{args.gpus}", "layout": "packed [T, H, d]",
+            "l2": "inputs larger than L2" if 8 * T * H * d * 2 > 129e6 else "L2-resident"}
+
+
+def run_varlen(args):
+    """One step = fa_fwd_varlen + fa_bwd_varlen over a packed batch of seeded
+    variable-length sequences (the same lengths for queries and keys)."""
+    import torch
+
+    import exact_tiled_attention_28_gb300 as fa
+    from exact_tiled_attention_28_gb300 import inputs, replicas
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    fa.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    S, H, d = VARLEN_WORKLOADS[args.workload][:3]
+    lengths = varlen_lengths(args.workload)
+    causal = bool(args.causal)
+    scale = 1.0 / math.sqrt(d)
+    seed = replicas.replica_seed(1000, rank)
+    bits, cu_q, cu_k = inputs.packed_inputs(seed, lengths, lengths, H, d)
+    T = int(cu_q[-1])
+    host = {n: inputs.bits_to_torch_bf16(b).pin_memory() for n, b in bits.items()}
+    x = {n: t.to(dev) for n, t in host.items()}
+    cu = torch.tensor(cu_q, dtype=torch.int32, device=dev)
+    mx = max(lengths)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_varlen_workspace_size(S, H, T, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def compute(xb, ob, wb, st):
+        fa.fa_fwd_varlen(xb["q"], xb["k"], xb["v"], ob["o"], ob["lse"], cu, cu, mx, mx, causal,
+                         scale, stream=st)
+        fa.fa_bwd_varlen(xb["q"], xb["k"], xb["v"], ob["o"], ob["lse"], xb["do"], ob["dq"],
+                         ob["dk"], ob["dv"], cu, cu, mx, mx, causal, scale, wb, stream=st)
+
+    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd_varlen(x["q"], x["k"], x["v"], o, lse, cu, cu, mx, mx, causal, scale)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_varlen(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, cu, cu, mx, mx,
+                         causal, scale, ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status reports an error during warm-up")
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status reports an error in the timed region")
+    ms_step = t_start.elapsed_time(t_end) / args.steps
+    ms_step_max = replicas.max_over_ranks(ms_step, dev)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    e2e_ms, h2d, d2h, h2d_gbs, d2h_gbs = run_e2e(fa, torch, host, x, o, lse, dq, dk, dv, ws,
+                                                 causal, scale, args.e2e_steps, compute=compute)
+    F = sum(fwd_flops(1, H, n, d, causal) for n in lengths)
+    peaks = load_peaks()
+    tag = "of " + peaks["source"]
+    value = replicas.aggregate_throughput(3.5 * F, world, ms_step_max)
+    bwd_tf = 2.5 * F / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = F / (fwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: Q, K, V, dO i.i.d. N(0,1) rounded to bf16, seeded; seeded lengths",
+        "config": varlen_config_of(args, lengths, H, d),
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_burst_peak": fwd_tf / peaks["burst"],
+                "frac_of_sustained_peak": fwd_tf / peaks["sustained"]},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf},
+        "roofline": {"kernel": "fa_bwd_varlen (all stages)", "bound": "tensor",
+                     "achieved": bwd_tf, "peak": peaks["sustained"], "unit": "TFLOP/s",
+                     "frac": bwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}",
+                     "traffic": None,
+                     "algorithmic": f"2.5 x sum_b 4*H*n_b^2*d{' / 2' if causal else ''} = "
+                                    f"{2.5 * F:.4g} FLOP per launch"},
+        "roofline_fwd": {"kernel": "fwd_kernel (packed batch)", "bound": "tensor",
+                         "achieved": fwd_tf, "peak": peaks["sustained"], "unit": "TFLOP/s",
+                         "frac": fwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}"},
+        "e2e": {"value": 3.5 * F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipelined": "copy-in, compute and copy-out streams, double-buffered",
+                "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs},
+        # per step: check + forward, check + pre-pass + dK/dV + dQ convert
+        "gpu_launches": 6 * args.steps,
+        "clocks": clocks,
+    }
+    if world > 1:
+        torch.distributed.barrier()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, heads, spent = oracle_sample(S, H, mx, d, causal, seed, args.cpu_budget_s, 64, lengths)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"{heads} whole (sequence, head) blocks fwd+bwd, "
+                                          f"{spent:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
 
 
 def run_ours(args):
@@ -428,6 +604,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in VARLEN_WORKLOADS:
+        run_varlen(args)
     else:
         run_ours(args)
 

@@ -17,6 +17,8 @@ from .binding import (  # noqa: F401
     fa_bwd_varlen,
     fa_bwd_varlen_workspace_size,
     fa_bwd_workspace_size,
+    fa_decode,
+    fa_decode_workspace_size,
     fa_fwd,
     fa_fwd_varlen,
     fa_last_device_status,

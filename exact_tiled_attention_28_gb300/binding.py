@@ -26,7 +26,8 @@ EXPORTED = ("fa_abi_version", "fa_fwd", "fa_fwd_strided", "fa_bwd_workspace_size
             "fa_bwd_strided", "fa_bwd_preprocess",
             "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout", "fa_selftest_exp2",
             "fa_status_string", "fa_last_device_status", "fa_fwd_nqnk", "fa_bwd_nqnk",
-            "fa_fwd_varlen", "fa_bwd_varlen_workspace_size", "fa_bwd_varlen")
+            "fa_fwd_varlen", "fa_bwd_varlen_workspace_size", "fa_bwd_varlen",
+            "fa_decode_workspace_size", "fa_decode")
 
 # fixed device scratch of fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in include/fa.h)
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -94,6 +95,10 @@ def load():
     lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd_varlen.restype = i
     lib.fa_bwd_varlen.argtypes = [vp] * 11 + [i] * 7 + [ll, i, f, vp, sz, vp]
+    lib.fa_decode_workspace_size.restype = sz
+    lib.fa_decode_workspace_size.argtypes = [i] * 5
+    lib.fa_decode.restype = i
+    lib.fa_decode.argtypes = [vp] * 6 + [i] * 5 + [ll, i, f, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -395,3 +400,38 @@ def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
                                 Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), d, st,
                                 int(bool(causal)), float(scale), workspace.data_ptr(),
                                 workspace.numel(), _stream_handle(stream)), "fa_bwd_varlen")
+
+
+# ---------------------------------------------------------------------------
+# decode against a key/value cache
+
+def fa_decode_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().fa_decode_workspace_size(B, H, Nq, Nk, d))
+
+
+def fa_decode(q, k_cache, v_cache, o, lse, causal: bool, scale: float, cache_seqlens=None,
+              workspace=None, stream=None) -> None:
+    """o, lse <- attention of Nq <= 16 new rows per (batch, head) against the
+    cache: q, o [B, H, Nq, d] and k_cache, v_cache [B, H, Nk, d] bf16 views
+    with a contiguous last dimension (a [B, Nk, H, d] cache passed as
+    .transpose(1, 2) is fine); lse fp32 [B, H, Nq]; cache_seqlens an int32
+    CUDA tensor of B valid key counts, or None; workspace a CUDA uint8 tensor
+    of fa_decode_workspace_size(...) bytes."""
+    import torch
+    B, H, Nq, d = _shape(q)
+    Nk = int(k_cache.shape[2]) if k_cache.dim() == 4 else -1
+    bf = torch.bfloat16
+    ts = ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (o, "o"))
+    ptrs = [_dev_ptr(t, n, bf, (B, H, Nk if n.endswith("cache") else Nq, d), strided=True)
+            for t, n in ts]
+    pl = _dev_ptr(lse, "lse", torch.float32, (B, H, Nq))
+    cs = 0
+    if cache_seqlens is not None:
+        cs = _dev_ptr(cache_seqlens, "cache_seqlens", torch.int32, (B,))
+    wp, wn = 0, 0
+    if workspace is not None:
+        _check_workspace(workspace)
+        wp, wn = workspace.data_ptr(), workspace.numel()
+    st = _strides([t for t, _ in ts])
+    _check(load().fa_decode(*ptrs, pl, cs or None, B, H, Nq, Nk, d, st, int(bool(causal)),
+                            float(scale), wp or None, wn, _stream_handle(stream)), "fa_decode")

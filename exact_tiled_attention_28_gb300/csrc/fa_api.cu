@@ -3,6 +3,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -452,6 +453,46 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
   s = fa::check_ptrs({q, k, v, o, lse, dO, dq, dk, dv});
   if (s != FA_OK) return s;
   return var_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
+  if (fa::check_sizes(B, H, Nq, d, 1.f) != FA_OK || Nq > fa::kDecodeMaxQ || Nk < 1) return 0;
+  // an upper bound over devices of up to 1024 SMs; a call needs at most this
+  return std::max<size_t>(fa::decode_workspace_bytes(B, H, Nq, Nk, d, 1024), 16);
+}
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    const int* cache_seqlens, int B, int H, int Nq, int Nk, int d,
+                    const long long* strides, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  fa_status s = fa::check_sizes(B, H, Nq, d, scale);
+  if (s != FA_OK) return s;
+  if (Nq > fa::kDecodeMaxQ) return FA_ERR_UNSUPPORTED;
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  s = fa::check_ptrs({q, k_cache, v_cache, o, lse});
+  if (s != FA_OK) return s;
+  if (cache_seqlens != nullptr && (reinterpret_cast<uintptr_t>(cache_seqlens) & 3u) != 0)
+    return FA_ERR_INVALID_ARG;
+  if (strides != nullptr) {
+    s = fa::check_strides(strides, 4);
+    if (s != FA_OK) return s;
+  }
+  fa::DeviceInfo di;
+  if (fa::device_info(&di) != cudaSuccess) return FA_ERR_CUDA;
+  const size_t need = fa::decode_workspace_bytes(B, H, Nq, Nk, d, di.num_sms);
+  if (need > 0 && (workspace == nullptr || !fa::aligned16(workspace) || workspace_bytes < need))
+    return FA_ERR_WORKSPACE;
+  fa::Problem p{B, H, Nq, d, causal ? 1 : 0, scale, di.num_sms, di.status, {}};
+  for (int t = 0; t < fa::kNumTensors; ++t) {
+    const bool kv = t == fa::kK || t == fa::kV;
+    p.st[t] = (strides != nullptr && t < 4)
+                  ? fa::Strides{strides[3 * t], strides[3 * t + 1], strides[3 * t + 2]}
+                  : fa::contiguous_strides(H, kv ? Nk : Nq, d);
+  }
+  p.Nk = Nk;
+  const cudaError_t e = fa::launch_decode(p, q, k_cache, v_cache, o, lse, cache_seqlens,
+                                          workspace, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_selftest_wait_timeout(int limit_ms, void* stream) {

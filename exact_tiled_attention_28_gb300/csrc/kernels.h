@@ -64,6 +64,24 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
 
 size_t bwd_workspace_bytes(int B, int H, int N, int d);
 
+// Decode: Nq <= kDecodeMaxQ new query rows per (batch, head) against a cache
+// of up to Nk keys (cache_seqlens[b] of them when given), split along the
+// keys over CTAs and merged by log-sum-exp.
+constexpr int kDecodeMaxQ = 16;
+
+struct DecodePlan {
+  int splits;           // key splits per (batch, head)
+  int tiles_per_split;  // 128-key tiles per split
+};
+
+DecodePlan decode_plan(int B, int H, int Nk, int num_sms);
+size_t decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_sms);
+
+// p.N = Nq, p.Nk = Nk; p.st holds the strides of q, k, v, o (kQ .. kO).
+cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                          float* lse, const int* cache_seqlens, void* workspace,
+                          cudaStream_t stream);
+
 // Workspace of the backward for unequal lengths (packed = false: B dense
 // sequences of rows_q query rows) or a packed batch of B sequences with
 // rows_q query rows in all: D and the log2 LSE rows (fp32) padded per

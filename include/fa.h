@@ -189,6 +189,34 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         size_t workspace_bytes, void* stream);
 
 /*
+ * Decode: Nq new query rows (1 <= Nq <= 16) of each of B sequences and H
+ * heads against a key/value cache, the serving use the pages name
+ * ("flashattention-2" glossary, "Adoption": vLLM's attention backend;
+ * "Flash Attention v2" notes, "Performance Comparison: v1 vs v2": 256-token
+ * generation). Computes o and lse exactly as fa_fwd_nqnk would, with the
+ * keys of each (batch, head) split over several thread blocks and the parts
+ * merged by their log-sum-exp (the identity behind the online softmax,
+ * "Flash Attention v2" notes, "Detailed Algorithm Comparison", forward pass).
+ *  q, o: bf16 [B, H, Nq, d]; k_cache, v_cache: bf16 [B, H, Nk, d]; strides: 12
+ *  element strides (batch, head, row) for q, k_cache, v_cache, o as in
+ *  fa_fwd_strided (a [B, Nk, H, d] cache is a view), or NULL for contiguous
+ *  tensors. lse: fp32 [B, H, Nq].
+ *  cache_seqlens: NULL (every sequence has Nk keys) or a DEVICE int32 array
+ *  of B valid key counts in 0..Nk; the causal mask is aligned at the bottom
+ *  right of each sequence's keys (row r sees key j <= r + nk - Nq). Counts
+ *  outside 0..Nk are clamped and reported as FA_ERR_INVALID_ARG by the next
+ *  fa_last_device_status(). Rows that see no key get o = 0, lse = -inf.
+ *  workspace: device memory of fa_decode_workspace_size() bytes, 16-byte
+ *  aligned (NULL is accepted when that size is 16 or less and the call needs
+ *  none). Nq > 16 returns FA_ERR_UNSUPPORTED (use fa_fwd_nqnk).
+ */
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d);
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    const int* cache_seqlens, int B, int H, int Nq, int Nk, int d,
+                    const long long* strides, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
  * Self-test of the failure path (no counterpart in the method): enqueues a
  * one-thread kernel that waits on an on-chip barrier nothing ever arrives on,
  * with a limit of limit_ms milliseconds (1..2000) instead of the 2 s the
@@ -238,7 +266,8 @@ const char* fa_status_string(int status);
  * Synchronises the stream, then returns FA_ERR_TIMEOUT if any kernel of this
  * process has recorded a bounded-wait timeout since the last call,
  * FA_ERR_INVALID_ARG if a packed batch's offsets broke the rules of
- * fa_fwd_varlen (the first such record wins; the call clears it),
+ * fa_fwd_varlen or a decode cache length was outside 0..Nk (the first such
+ * record wins; the call clears it),
  * FA_ERR_CUDA if the synchronisation failed, else FA_OK.
  */
 fa_status fa_last_device_status(void* stream);

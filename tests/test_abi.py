@@ -183,3 +183,19 @@ def test_varlen_entry_points_reject_before_launch(lib):
                              None) == fa.FA_ERR_WORKSPACE
     assert lib.fa_bwd_varlen(*([P] * 11), 3, 2, 500, 700, 300, 400, 128, None, 0, 0.1, None, ws,
                              None) == fa.FA_ERR_WORKSPACE
+
+
+def test_decode_rejects_before_launch(lib):
+    def dec(q=P, cs=None, B=2, H=4, Nq=1, Nk=1000, d=128, st=None, scale=0.1):
+        return lib.fa_decode(q, P, P, P, P, cs, B, H, Nq, Nk, d, st, 1, scale, None, 0, None)
+
+    assert dec(q=None) == fa.FA_ERR_INVALID_ARG
+    assert dec(Nq=17) == fa.FA_ERR_UNSUPPORTED
+    assert dec(Nq=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(Nk=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert dec(cs=P + 2) == fa.FA_ERR_INVALID_ARG
+    assert dec(scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert dec(st=(ctypes.c_longlong * 12)(*([64] * 11 + [3]))) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_decode_workspace_size(1, 1, 1, 1 << 17, 128) >= 152 * (128 + 1) * 4
+    assert fa.fa_decode_workspace_size(1, 1, 17, 1000, 128) == 0

@@ -1,0 +1,113 @@
+"""Decode parity: Nq <= 16 new rows per (batch, head) against a key/value cache
+through fa_decode, against the fp64 oracle on each sequence's valid keys
+(causal mask aligned at the bottom right). Covers one split and many splits
+per head, per-sequence cache lengths (including 0 and fewer keys than
+queries), a [B, Nk, H, d] cache layout and every head dimension.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_tiled_attention_28_gb300 import inputs
+
+from . import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode(fa, seed, B, H, Nq, Nk, d, causal, seqlens=None, bnhd=False, scale=None):
+    import torch
+    scale = gu.default_scale(d) if scale is None else scale
+    bits = inputs.nqnk_inputs(seed, B, H, Nq, Nk, d)
+    dev = {n: inputs.bits_to_torch_bf16(b).cuda() for n, b in bits.items()}
+    x = {n: inputs.bf16_bits_to_f64(b) for n, b in bits.items()}
+    k, v = dev["k"], dev["v"]
+    if bnhd:  # the cache stored as [B, Nk, H, d]
+        k = k.transpose(1, 2).contiguous().transpose(1, 2)
+        v = v.transpose(1, 2).contiguous().transpose(1, 2)
+    o = torch.full_like(dev["q"], float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    cs = None if seqlens is None else torch.tensor(seqlens, dtype=torch.int32, device="cuda")
+    ws = torch.full((fa.fa_decode_workspace_size(B, H, Nq, Nk, d),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    fa.fa_decode(dev["q"], k, v, o, lse, causal, scale, cache_seqlens=cs, workspace=ws)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    og, lg = gu.to_f64(o), gu.to_f64(lse)
+    what = f"B={B} H={H} Nq={Nq} Nk={Nk} d={d} causal={causal} seqlens={seqlens}"
+    for b in range(B):
+        nk = Nk if seqlens is None else seqlens[b]
+        for h in range(H):
+            ow, lw = oracle.head_forward(x["q"][b, h], x["k"][b, h, :nk], x["v"][b, h, :nk],
+                                         causal, scale)
+            empty = np.isneginf(lw)
+            assert np.array_equal(np.isneginf(lg[b, h]), empty), what
+            assert np.all(og[b, h][empty] == 0.0), what
+            if np.any(~empty):
+                gu.check_o_lse(og[b, h][~empty], lg[b, h][~empty], ow[~empty], lw[~empty],
+                               f"{what} b={b} h={h}")
+    return o, lse
+
+
+@pytest.mark.parametrize("Nq", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_many_splits(cuda_lib, Nq, causal):
+    """Two heads: the keys of each are split over many CTAs."""
+    _decode(cuda_lib, 500 + Nq, 1, 2, Nq, 5000, 128, causal)
+
+
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_head_dims_and_cache_lengths(cuda_lib, d, causal):
+    """Per-sequence cache lengths: 0 (no key), fewer keys than queries, a
+    ragged tile, exactly one tile, the whole cache."""
+    _decode(cuda_lib, 510 + d, 5, 3, 4, 1000, d, causal, seqlens=[0, 2, 129, 128, 1000])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_one_split_per_head(cuda_lib, causal):
+    """More heads than SMs: one CTA per head writes O and LSE directly."""
+    _decode(cuda_lib, 520, 8, 24, 1, 700, 128, causal)
+    _decode(cuda_lib, 521, 8, 24, 2, 300, 64, causal)
+
+
+def test_decode_cache_layout_bnhd(cuda_lib):
+    _decode(cuda_lib, 530, 3, 4, 2, 2000, 128, True, seqlens=[2000, 1, 777], bnhd=True)
+
+
+def test_decode_matches_nqnk_path(cuda_lib):
+    """The split decode and the tensor-core path for Nq != Nk compute the same
+    function: their outputs agree to bf16 rounding."""
+    import torch
+    fa = cuda_lib
+    B, H, Nq, Nk, d = 2, 4, 8, 3000, 128
+    bits = inputs.nqnk_inputs(540, B, H, Nq, Nk, d)
+    dev = {n: inputs.bits_to_torch_bf16(b).cuda() for n, b in bits.items()}
+    for causal in (False, True):
+        o1 = torch.empty_like(dev["q"])
+        l1 = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+        o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+        ws = torch.empty(fa.fa_decode_workspace_size(B, H, Nq, Nk, d), dtype=torch.uint8,
+                         device="cuda")
+        fa.fa_decode(dev["q"], dev["k"], dev["v"], o1, l1, causal, 0.1, workspace=ws)
+        fa.fa_fwd(dev["q"], dev["k"], dev["v"], o2, l2, causal, 0.1)
+        assert fa.fa_last_device_status() == fa.FA_OK
+        assert gu.max_abs(gu.to_f64(l1), gu.to_f64(l2)) < 1e-4
+        assert gu.rel_l2(gu.to_f64(o1), gu.to_f64(o2)) < 5e-3
+
+
+def test_decode_cache_length_out_of_range_is_reported(cuda_lib):
+    import torch
+    fa = cuda_lib
+    bits = inputs.nqnk_inputs(550, 2, 2, 1, 300, 64)
+    dev = {n: inputs.bits_to_torch_bf16(b).cuda() for n, b in bits.items()}
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty((2, 2, 1), dtype=torch.float32, device="cuda")
+    ws = torch.empty(fa.fa_decode_workspace_size(2, 2, 1, 300, 64), dtype=torch.uint8,
+                     device="cuda")
+    cs = torch.tensor([300, 301], dtype=torch.int32, device="cuda")
+    fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, True, 0.1, cache_seqlens=cs, workspace=ws)
+    assert fa.fa_last_device_status() == fa.FA_ERR_INVALID_ARG
+    cs = torch.tensor([300, 299], dtype=torch.int32, device="cuda")
+    fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, True, 0.1, cache_seqlens=cs, workspace=ws)
+    assert fa.fa_last_device_status() == fa.FA_OK

@@ -80,3 +80,38 @@ def test_key_block_order_is_free(causal):
     b = tiled_forward(t["q"], t["k"], t["v"], causal, 0.4, 16, 16, reverse_kv=True)
     assert np.max(np.abs(a[0] - b[0])) < 1e-12
     assert np.max(np.abs(a[1] - b[1])) < 1e-12
+
+
+def test_key_splits_merged_by_log_sum_exp():
+    """Splitting the keys into contiguous ranges, attending to each range
+    alone and merging the parts with weights exp(LSE_s - LSE), LSE = ln sum_s
+    exp(LSE_s), gives the whole attention: the identity the decode path's
+    split-KV merge rests on. Ranges that no query can see (LSE_s = -inf)
+    weigh nothing."""
+    t = pins._head_pair(131, 3, 700, 16)
+    for causal in (False, True):
+        O, lse = oracle.head_forward(t["q"], t["k"], t["v"], causal, 0.3)
+        parts = []
+        for k0, k1 in ((0, 128), (128, 300), (300, 301), (301, 700)):
+            kk, vv = t["k"][:k1], t["v"][:k1]
+            # the range's own attention: keys outside [k0, k1) masked out, with
+            # the causal alignment of the whole key set
+            Os, ls = oracle.head_forward(t["q"], kk[k0:], vv[k0:], False, 0.3)
+            if causal:
+                keep = np.arange(k0, k1)[None, :] <= np.arange(3)[:, None] + 700 - 3
+                S = 0.3 * t["q"] @ kk[k0:].T
+                S = np.where(keep, S, -np.inf)
+                m = np.max(S, axis=1, keepdims=True)
+                fin = np.isfinite(m[:, 0])
+                E = np.exp(S - np.where(np.isfinite(m), m, 0.0))
+                l = E.sum(axis=1)
+                Os = np.where(fin[:, None], (E @ vv[k0:]) / np.where(l > 0, l, 1.0)[:, None], 0.0)
+                with np.errstate(divide="ignore"):
+                    ls = np.where(fin, m[:, 0] + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+            parts.append((Os, ls))
+        L = np.stack([p[1] for p in parts])
+        M = L.max(axis=0)
+        W = np.exp(L - M)
+        lse_m = M + np.log(W.sum(axis=0))
+        O_m = sum(w[:, None] * p[0] for w, p in zip(W, parts)) / W.sum(axis=0)[:, None]
+        assert np.max(np.abs(O_m - O)) < 1e-12 and np.max(np.abs(lse_m - lse)) < 1e-12
