@@ -52,6 +52,22 @@ VARLEN_WORKLOADS = {"varlen_d128_s16_256to4096": (16, 16, 128, 256, 4096, 7),
                     "varlen_d64_s64_64to1024": (64, 32, 64, 64, 1024, 8)}
 
 
+# Decode against a key/value cache (fa_decode): name -> (B, H, Nq, Nk, d);
+# the cache is [B, Nk, H, d] and sequence b holds a seeded number of valid
+# keys in [Nk / 2, Nk] (cache_seqlens). Timed metric: cache bytes read per
+# second; one step = one fa_decode call.
+DECODE_WORKLOADS = {"decode_b32_h32_nq1_nk8192_d128": (32, 32, 1, 8192, 128),
+                    "decode_b1_h32_nq1_nk131072_d128": (1, 32, 1, 131072, 128),
+                    "decode_b32_h32_nq4_nk8192_d128": (32, 32, 4, 8192, 128)}
+DECODE_METRIC = "attention decode: KV-cache GB/s read (bf16, 1 GB300)"
+
+
+def decode_lengths(name):
+    import numpy as np
+    B, _, _, Nk, _ = DECODE_WORKLOADS[name]
+    return [int(n) for n in np.random.default_rng(9).integers(Nk // 2, Nk + 1, size=B)]
+
+
 def varlen_lengths(name):
     import numpy as np
     S, _, _, lo, hi, seed = VARLEN_WORKLOADS[name]
@@ -177,7 +193,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(VARLEN_WORKLOADS) + sorted(DECODE_WORKLOADS))
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--layout", default="bhnd", choices=("bhnd", "bnhd"),
                     help="memory layout of q, k, v, o, dO and the gradients")
@@ -208,6 +224,28 @@ def run_reference(args):
     """The reference arm: the fp64 oracle as it stands, on the host cores."""
     world, rank, _ = dist_setup(args)
     if rank != 0:
+        return
+    if args.workload in DECODE_WORKLOADS:
+        B, H, Nq, Nk, d = DECODE_WORKLOADS[args.workload]
+        dl = decode_lengths(args.workload)
+        for _ in range(args.warmup):
+            decode_oracle_sample(B, H, Nq, Nk, d, args.causal, dl, 1000, 0.0, 1)
+        nbytes, spent = 0.0, 0.0
+        for _ in range(args.steps):
+            g, _, sp = decode_oracle_sample(B, H, Nq, Nk, d, args.causal, dl, 1000, 0.0, 1)
+            nbytes += g * 1e9 * sp
+            spent += sp
+        value = nbytes / spent / 1e9
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": spent * 1e3 / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": decode_config_of(args, B, H, Nq, Nk, d, dl),
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(),
+                                 "kind": "oracle", "sample": "one (sequence, head) block per step"},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     lengths = None
     if args.workload in VARLEN_WORKLOADS:
@@ -448,6 +486,156 @@ def run_varlen(args):
         torch.distributed.destroy_process_group()
 
 
+def decode_config_of(args, B, H, Nq, Nk, d, lengths):
+    return {"workload": f"{args.workload}: B={B} H={H} Nq={Nq} cache Nk={Nk} d={d} "
+                        f"(valid keys {min(lengths)}..{max(lengths)} per sequence), "
+                        f"{'causal' if args.causal else 'non-causal'}, forward",
+            "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": bool(args.causal),
+            "scale": "1/sqrt(d)", "global_batch": B * args.gpus, "seq_len": Nk,
+            "parallelism": f"replicas x{args.gpus}", "layout": "cache [B, Nk, H, d]",
+            "l2": "cache larger than L2" if 2 * sum(lengths) * H * d * 2 > 129e6 else "L2-resident"}
+
+
+def decode_oracle_sample(B, H, Nq, Nk, d, causal, lengths, seed, budget_s, max_heads):
+    """The oracle on whole (sequence, head) blocks; returns (cache GB/s, heads, s)."""
+    import oracle
+    from exact_tiled_attention_28_gb300 import inputs
+    scale = 1.0 / math.sqrt(d)
+    heads, spent, nbytes = 0, 0.0, 0
+    while heads < max_heads and (heads == 0 or spent < budget_s):
+        b, h = divmod(heads % (B * H), H)
+        n = lengths[b]
+        x = inputs.head_inputs_f64(seed, b, h, Nq, d, ("q",))
+        kv = inputs.head_inputs_f64(seed + inputs.KV_SEED_OFFSET, b, h, Nk, d, ("k", "v"))
+        t0 = time.perf_counter()
+        oracle.head_forward(x["q"], kv["k"][:n], kv["v"][:n], causal, scale)
+        spent += time.perf_counter() - t0
+        nbytes += 2 * n * d * 2
+        heads += 1
+    return nbytes / spent / 1e9, heads, spent
+
+
+def run_decode(args):
+    """One step = one fa_decode call over the workload's cache."""
+    import torch
+
+    import exact_tiled_attention_28_gb300 as fa
+    from exact_tiled_attention_28_gb300 import inputs, replicas
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    fa.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, H, Nq, Nk, d = DECODE_WORKLOADS[args.workload]
+    lengths = decode_lengths(args.workload)
+    causal = bool(args.causal)
+    scale = 1.0 / math.sqrt(d)
+    seed = replicas.replica_seed(1000, rank)
+    bits = inputs.nqnk_inputs(seed, B, H, Nq, Nk, d)
+    # the cache stored as [B, Nk, H, d], passed as [B, H, Nk, d] views
+    k = inputs.bits_to_torch_bf16(bits["k"]).to(dev).transpose(1, 2).contiguous().transpose(1, 2)
+    v = inputs.bits_to_torch_bf16(bits["v"]).to(dev).transpose(1, 2).contiguous().transpose(1, 2)
+    del bits["k"], bits["v"]
+    q_host = inputs.bits_to_torch_bf16(bits["q"]).pin_memory()
+    q = q_host.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    cs = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(fa.fa_decode_workspace_size(B, H, Nq, Nk, d), 16), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_decode(q, k, v, o, lse, causal, scale, cache_seqlens=cs, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status reports an error during warm-up")
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status reports an error in the timed region")
+    ms_step = t_start.elapsed_time(t_end) / args.steps
+    ms_step_max = replicas.max_over_ranks(ms_step, dev)
+    kv_bytes = 2 * sum(lengths) * H * d * 2
+    algo_bytes = kv_bytes + 2 * (B * H * Nq * d * 2) + B * H * Nq * 4  # + q, o, lse
+    # end to end: each step copies its new query rows in and o, lse out (pinned
+    # host memory); the cache stays resident on the device
+    o_host = torch.empty_like(o, device="cpu").pin_memory()
+    l_host = torch.empty_like(lse, device="cpu").pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(args.e2e_steps, 1)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n_e2e):
+        q.copy_(q_host, non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+        l_host.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    peaks = load_peaks()
+    gbs = kv_bytes / (ms_step_max * 1e-3) / 1e9 * world
+    achieved = algo_bytes / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: q, K, V i.i.d. N(0,1) rounded to bf16, seeded; seeded cache lengths",
+        "config": decode_config_of(args, B, H, Nq, Nk, d, lengths),
+        "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel", "bound": "hbm",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "peak_kind": f"copy bandwidth of {peaks['source']}", "traffic": None,
+                     "algorithmic": f"K and V of the valid keys once, q, o, lse: {algo_bytes:.4g} "
+                                    f"bytes per call"},
+        "tflops": 4.0 * Nq * sum(lengths) * H * d / (ms_step * 1e-3) / 1e12,
+        "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+                "note": "the cache stays on the device; each step copies q in and o, lse out"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if world > 1:
+        torch.distributed.barrier()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_, heads, spent = decode_oracle_sample(B, H, Nq, Nk, d, causal, lengths, seed,
+                                                args.cpu_budget_s, 512)
+        line["cpu_baseline"] = {"value": v_, "unit": "GB/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"{heads} whole (sequence, head) blocks, {spent:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def run_ours(args):
     import torch
 
@@ -606,6 +794,8 @@ def main():
         run_reference(args)
     elif args.workload in VARLEN_WORKLOADS:
         run_varlen(args)
+    elif args.workload in DECODE_WORKLOADS:
+        run_decode(args)
     else:
         run_ours(args)
 

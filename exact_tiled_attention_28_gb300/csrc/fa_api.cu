@@ -457,8 +457,17 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
 
 size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
   if (fa::check_sizes(B, H, Nq, d, 1.f) != FA_OK || Nq > fa::kDecodeMaxQ || Nk < 1) return 0;
-  // an upper bound over devices of up to 1024 SMs; a call needs at most this
-  return std::max<size_t>(fa::decode_workspace_bytes(B, H, Nq, Nk, d, 1024), 16);
+  // the plan depends on the SM count: the current device's, else the most
+  // any plan can use (every split count up to kDecodeMaxSplits)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+    return std::max<size_t>(fa::decode_workspace_bytes(B, H, Nq, Nk, d, sms), 16);
+  cudaGetLastError();  // no device here: clear the error
+  int nqp = 1;
+  while (nqp < Nq) nqp *= 2;
+  const size_t splits = std::min((Nk + fa::kTile - 1) / fa::kTile, fa::kDecodeMaxSplits);
+  return std::max<size_t>(static_cast<size_t>(B) * H * splits * nqp * (d + 1) * 4, 16);
 }
 
 fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,

@@ -68,6 +68,7 @@ size_t bwd_workspace_bytes(int B, int H, int N, int d);
 // of up to Nk keys (cache_seqlens[b] of them when given), split along the
 // keys over CTAs and merged by log-sum-exp.
 constexpr int kDecodeMaxQ = 16;
+constexpr int kDecodeMaxSplits = 256;
 
 struct DecodePlan {
   int splits;           // key splits per (batch, head)
