@@ -65,10 +65,16 @@ cudaError_t device_info(DeviceInfo* out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-fa_status check_sizes(int B, int H, int N, int d, float scale) {
+// allow256: the forward of dense (or strided) equal-length batches also takes
+// d = 256; nothing else does.
+fa_status check_sizes(int B, int H, int N, int d, float scale, bool allow256 = false) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * H >= (int64_t(1) << 31)) return FA_ERR_UNSUPPORTED;
-  if (d != 32 && d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128 && !(allow256 && d == 256))
+    return FA_ERR_UNSUPPORTED;
+  if (allow256 && d == 256 &&
+      static_cast<int64_t>(B) * H * ((N + kTile - 1) / kTile) >= (int64_t(1) << 31))
+    return FA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
@@ -173,7 +179,7 @@ const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null or misaligned pointer, size < 1 or bad scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension must be 32, 64, 96 or 128";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension or size not supported by this call";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side bounded wait expired";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: backward workspace null or too small";
@@ -188,7 +194,7 @@ namespace {
 fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int N, int d, const long long* strides, int causal, float scale,
                      void* stream) {
-  fa_status s = fa::check_sizes(B, H, N, d, scale);
+  fa_status s = fa::check_sizes(B, H, N, d, scale, /*allow256=*/true);
   if (s != FA_OK) return s;
   s = fa::check_ptrs({q, k, v, o, lse});
   if (s != FA_OK) return s;

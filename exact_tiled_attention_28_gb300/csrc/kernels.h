@@ -55,6 +55,10 @@ bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int 
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream);
 
+// Forward at head dimension 256 (dense or strided [B, H, N, d], equal lengths).
+cudaError_t launch_fwd256(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                          float* lse, cudaStream_t stream);
+
 // The backward's three stages; pointers the stage does not use may be null.
 enum BwdStage : int { kStagePre = 1, kStageDkdv = 2, kStageDq = 4, kStagesAll = 7 };
 

@@ -23,7 +23,10 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
  *    aligned. The library keeps no reference to them after the call.
  *  - d must be 32, 64, 96 or 128; B, H, N >= 1; B*H < 2^31 (offsets are computed in
- *    64 bits, so a tensor may hold more than 2^31 elements).
+ *    64 bits, so a tensor may hold more than 2^31 elements). fa_fwd and
+ *    fa_fwd_strided also take d = 256 ("Flash Attention v2" notes,
+ *    "Detailed Differences", 3 "Head Dimension Support"); no other entry
+ *    point does (FA_ERR_UNSUPPORTED).
  *  - Causal masking is top-left aligned with equal query and key lengths:
  *    query i sees keys j <= i. scale must be finite and >= 0.
  *  - stream is a cudaStream_t (NULL = the legacy default stream). Every call
@@ -47,7 +50,7 @@ extern "C" {
 typedef enum fa_status {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, size < 1, bad scale */
-  FA_ERR_UNSUPPORTED = 2, /* head dimension not 32/64/96/128, or B*H too large */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension not supported by the call, or B*H too large */
   FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FA_ERR_TIMEOUT = 4,     /* a device-side bounded wait expired */
   FA_ERR_WORKSPACE = 5    /* backward workspace null or too small */

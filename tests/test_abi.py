@@ -77,7 +77,7 @@ def bwd(lib, ws=P, ws_bytes=None, B=1, H=1, N=128, d=64, scale=0.125, null=None)
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
     (dict(d=80), fa.FA_ERR_UNSUPPORTED),
     (dict(d=48), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
@@ -91,6 +91,7 @@ def test_bwd_rejects_before_launch(lib):
     for i in range(9):
         assert bwd(lib, null=i) == fa.FA_ERR_INVALID_ARG
     assert bwd(lib, d=48) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED  # d = 256 has a forward only
     assert bwd(lib, ws=None) == fa.FA_ERR_WORKSPACE
     assert bwd(lib, ws=P + 4) == fa.FA_ERR_WORKSPACE
     assert bwd(lib, ws_bytes=fa.fa_bwd_workspace_size(1, 1, 128, 64) - 1) == fa.FA_ERR_WORKSPACE
@@ -199,3 +200,16 @@ def test_decode_rejects_before_launch(lib):
     assert dec(st=(ctypes.c_longlong * 12)(*([64] * 11 + [3]))) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_decode_workspace_size(1, 1, 1, 1 << 17, 128) >= 152 * (128 + 1) * 4
     assert fa.fa_decode_workspace_size(1, 1, 17, 1000, 128) == 0
+
+
+def test_d256_is_forward_only(lib):
+    """d = 256 passes the forward's argument checks (on a host without a GPU
+    the call then fails at the device query, not as unsupported); every other
+    entry point rejects it."""
+    assert fwd(lib, d=256) != fa.FA_ERR_UNSUPPORTED
+    assert fwd(lib, d=256, q=None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_workspace_size(1, 1, 128, 256) == 0
+    assert lib.fa_fwd_nqnk(P, P, P, P, P, 1, 1, 10, 20, 256, None, 0, 0.1, None) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_decode(P, P, P, P, P, None, 1, 1, 1, 100, 256, None, 0, 0.1, None, 0, None) == \
+        fa.FA_ERR_UNSUPPORTED
