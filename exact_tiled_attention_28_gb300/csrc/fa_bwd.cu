@@ -18,10 +18,12 @@
 //     loops over the query blocks i (causal: i >= j, longest blocks first):
 //       S^T = K_j Q_i^T and dP^T = V_j dO_i^T       (tcgen05, SS)
 //       P^T, dS^T by two compute warpgroups, one thread per key row, each
-//       warpgroup owning 64 of the 128 query columns  (TMEM <-> regs)
-//       dV += P^T dO_i and dK += dS^T Q_i           (tcgen05, A from TMEM)
+//       warpgroup owning 64 of the 128 query columns  (TMEM -> regs; P^T
+//       back to TMEM, dS^T to swizzled shared memory)
+//       dV += P^T dO_i                              (tcgen05, A from TMEM)
 //       d >= 64: dQ_i^T = K_j^T dS^T (M = 128)      (tcgen05, both from SMEM)
 //       d = 32:  dQ_i = dS K_j                      (tcgen05, both from SMEM)
+//       dK += dS^T Q_i                              (tcgen05, both from SMEM)
 //     and four more warps read dQ_i out of TMEM and add it to the fp32
 //     accumulator in global memory. With dQ^T in TMEM (lanes = head dim,
 //     columns = queries) a warp's 32 atomics cover one contiguous 128-byte
@@ -30,9 +32,15 @@
 //
 // TMEM (512 columns): S^T [0,128), dP^T then dQ_i [128,256), dV [256, 256+d),
 // dK [256+d, 256+2d). Compute warpgroup c reads columns 64c..64c+63 of S^T and
-// dP^T and writes its packed bf16 P^T / dS^T (two per column) over the first 32
-// of those same columns, so neither warpgroup overwrites a column the other
-// still has to read; the MMAs address the two 32-column halves separately.
+// dP^T and writes its packed bf16 P^T (two per column) over the first 32 of
+// its S^T columns, so neither warpgroup overwrites a column the other still
+// has to read; the dV MMA addresses the two 32-column halves separately.
+// MMA order per query block, non-causal: dV(i), S^T(i+1), dQ(i), dK(i),
+// dP^T(i+1), with dK reading dS^T from shared memory: dQ_i comes before dK so
+// that its read-out from the dP^T columns overlaps the dK product (dP^T(i+1)
+// waits for that read-out). Causal: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1)
+// with dK reading dS^T from TMEM (the compute warps also store it there);
+// each order measured faster for its case on GB300 (by about 2.5%).
 
 #include <algorithm>
 
@@ -561,6 +569,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ts(dst, a_region + 64 * (kk >> 2) + 8 * (kk & 3), desc_at(db, kk * 2048), idesc_acc,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
+      // dK += dS^T Q: A = dS^T from shared memory (keys x queries, K-major,
+      // the buffer the dQ product reads too), B = Q_i MN-major. Reading dS^T
+      // from shared memory rather than TMEM frees the dP^T columns for dQ_i
+      // before dK is issued, so the dQ read-out overlaps the dK product.
+      auto issue_dk = [&](uint32_t q_tile, bool accumulate) {
+        const SmemDesc da = make_desc_sw128(opaque_u32(sDS), 16, 1024);
+        const SmemDesc db = make_desc_sw128(opaque_u32(q_tile), kBlk, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(tmem + Cfg::col_dk(), desc_at(da, (kk >> 2) * kBlk + (kk & 3) * 32),
+                 desc_at(db, kk * 2048), idesc_acc, (accumulate || kk > 0) ? 1u : 0u);
+      };
       auto issue_dq = [&]() {
         const SmemDesc d_ds = make_desc_sw128(opaque_u32(sDS), kBlk, 1024);
         const SmemDesc d_kmn = make_desc_sw128(opaque_u32(sK), kBlk, 1024);
@@ -628,9 +648,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = mbar_wait(smem_u32(&bars->ds_ready), it & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
-          issue_acc(tmem + Cfg::col_dk(), tmem + kColDP, stage, u > 0);  // dK += dS^T Q
-          issue_dq();                                                    // dQ_i = dS K
-          mma_commit(smem_u32(&bars->dq_full));
+          if constexpr (CAUSAL) {  // measured faster causal: dK first, dS^T from TMEM
+            issue_acc(tmem + Cfg::col_dk(), tmem + kColDP, stage, u > 0);  // dK += dS^T Q
+            issue_dq();                                                    // dQ_i = dS K
+            mma_commit(smem_u32(&bars->dq_full));
+          } else {
+            issue_dq();  // dQ_i = dS K, read out while dK runs
+            mma_commit(smem_u32(&bars->dq_full));
+            issue_dk(stage, u > 0);  // dK += dS^T Q
+          }
           mma_commit(smem_u32(&bars->st_empty[s]));
           if (!has_next) {
             mma_commit(smem_u32(&bars->acc_done));
@@ -754,7 +780,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float2 v = fmul2(pf, g);
             ds[c] = pack_bf16x2(v.x, v.y);
           }
-          tmem_st16(tDP + 16 * h, ds);
+          if constexpr (CAUSAL) tmem_st16(tDP + 16 * h, ds);  // the causal dK reads it there
 #pragma unroll
           for (int u4 = 0; u4 < 4; ++u4) {
             const int ch = 4 * h + u4;
