@@ -198,7 +198,7 @@ def parse_args():
     ap.add_argument("--layout", default="bhnd", choices=("bhnd", "bnhd"),
                     help="memory layout of q, k, v, o, dO and the gradients")
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -281,8 +281,12 @@ def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, st
             compute=None):
     """Times `steps` end-to-end steps (H2D of the inputs, fa_fwd + fa_bwd, D2H of
     every output) with the three stages pipelined across steps. ``compute(xb,
-    ob, wb, stream)`` replaces the fa_fwd + fa_bwd pair when given. Returns
-    (ms per step, H2D bytes, D2H bytes, H2D GB/s alone, D2H GB/s alone)."""
+    ob, wb, stream)`` replaces the fa_fwd + fa_bwd pair when given. The copies
+    in and the copies out each alternate over two streams: on GB300 the
+    host link carries about 205 GB/s in either direction alone and about 280
+    GB/s in both at once only with two streams per direction (one per
+    direction reached 245). Returns (ms per step, H2D bytes, D2H bytes, H2D
+    GB/s alone, D2H GB/s alone)."""
     outs0 = {"o": o0, "lse": lse0, "dq": dq0, "dk": dk0, "dv": dv0}
     bufs = [({n: t for n, t in x0.items()}, outs0, ws0),
             ({n: torch.empty_like(t) for n, t in x0.items()},
@@ -291,26 +295,32 @@ def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, st
                 for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs0.values())
-    s_in, s_out, s_comp = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.current_stream()
+    s_in = [torch.cuda.Stream(), torch.cuda.Stream()]
+    s_out = [torch.cuda.Stream(), torch.cuda.Stream()]
+    s_comp = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event()
-    in_done = [ev() for _ in range(steps)]
+    in_done = [[ev(), ev()] for _ in range(steps)]
     comp_done = [ev() for _ in range(steps)]
-    out_done = [ev() for _ in range(steps)]
+    out_done = [[ev(), ev()] for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record(s_comp)
-    s_in.wait_stream(s_comp)
+    for s in s_in + s_out:
+        s.wait_stream(s_comp)
     for k in range(steps):
         xb, ob, wb = bufs[k % 2]
-        with torch.cuda.stream(s_in):
-            if k >= 2:
-                s_in.wait_event(comp_done[k - 2])  # buffer k % 2 free for new inputs
-            for n in host:
-                xb[n].copy_(host[n], non_blocking=True)
-            in_done[k].record(s_in)
-        s_comp.wait_event(in_done[k])
+        for c, s in enumerate(s_in):
+            with torch.cuda.stream(s):
+                if k >= 2:
+                    s.wait_event(comp_done[k - 2])  # buffer k % 2 free for new inputs
+                for n in list(host)[c::2]:
+                    xb[n].copy_(host[n], non_blocking=True)
+                in_done[k][c].record(s)
+        for c in range(2):
+            s_comp.wait_event(in_done[k][c])
         if k >= 2:
-            s_comp.wait_event(out_done[k - 2])  # outputs k % 2 copied out
+            for c in range(2):
+                s_comp.wait_event(out_done[k - 2][c])  # outputs k % 2 copied out
         if compute is not None:
             compute(xb, ob, wb, s_comp)
         else:
@@ -318,12 +328,14 @@ def run_e2e(fa, torch, host, x0, o0, lse0, dq0, dk0, dv0, ws0, causal, scale, st
             fa.fa_bwd(xb["q"], xb["k"], xb["v"], ob["o"], ob["lse"], xb["do"], ob["dq"], ob["dk"],
                       ob["dv"], causal, scale, wb, stream=s_comp)
         comp_done[k].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[k])
-            for n, t in ob.items():
-                out_host[k % 2][n].copy_(t, non_blocking=True)
-            out_done[k].record(s_out)
-    s_comp.wait_event(out_done[steps - 1])
+        for c, s in enumerate(s_out):
+            with torch.cuda.stream(s):
+                s.wait_event(comp_done[k])
+                for n in list(ob)[c::2]:
+                    out_host[k % 2][n].copy_(ob[n], non_blocking=True)
+                out_done[k][c].record(s)
+    for c in range(2):
+        s_comp.wait_event(out_done[steps - 1][c])
     t1.record(s_comp)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
@@ -466,7 +478,7 @@ def run_varlen(args):
                          "frac": fwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}"},
         "e2e": {"value": 3.5 * F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelined": "copy-in, compute and copy-out streams, double-buffered",
+                "pipelined": "two copy-in streams, compute, two copy-out streams; double-buffered",
                 "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs},
         # per step: check + forward, check + pre-pass + dK/dV + dQ convert
         "gpu_launches": 6 * args.steps,
@@ -769,7 +781,7 @@ def run_ours(args):
                          "frac": fwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}"},
         "e2e": {"value": 3.5 * F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelined": "copy-in, compute and copy-out streams, double-buffered",
+                "pipelined": "two copy-in streams, compute, two copy-out streams; double-buffered",
                 "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
