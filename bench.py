@@ -424,7 +424,7 @@ def run_varlen(args):
     o = torch.empty_like(x["q"])
     lse = torch.empty((H, T), dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
-    ws = torch.empty(fa.fa_bwd_varlen_workspace_size(S, H, T, d), dtype=torch.uint8, device=dev)
+    ws = torch.empty(fa.fa_bwd_varlen_workspace_size(S, H, T, mx, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def compute(xb, ob, wb, st):

@@ -92,7 +92,7 @@ def load():
     lib.fa_fwd_varlen.restype = i
     lib.fa_fwd_varlen.argtypes = [vp] * 7 + [i] * 7 + [ll, i, f, vp]
     lib.fa_bwd_varlen_workspace_size.restype = sz
-    lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i, i]
     lib.fa_bwd_varlen.restype = i
     lib.fa_bwd_varlen.argtypes = [vp] * 11 + [i] * 7 + [ll, i, f, vp, sz, vp]
     lib.fa_decode_workspace_size.restype = sz
@@ -332,8 +332,8 @@ def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float,
 # ---------------------------------------------------------------------------
 # packed batches of variable-length sequences
 
-def fa_bwd_varlen_workspace_size(B: int, H: int, total_q: int, d: int) -> int:
-    return int(load().fa_bwd_varlen_workspace_size(B, H, total_q, d))
+def fa_bwd_varlen_workspace_size(B: int, H: int, total_q: int, max_seqlen_k: int, d: int) -> int:
+    return int(load().fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_k, d))
 
 
 def _varlen_args(q, k, v, tensors_q, tensors_k, cu_seqlens_q, cu_seqlens_k):
@@ -387,7 +387,7 @@ def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
                   stream=None) -> None:
     """dq, dk, dv <- gradients of sum(o * do) for a packed batch (see
     fa_fwd_varlen); workspace is a CUDA uint8 tensor of at least
-    fa_bwd_varlen_workspace_size(B, H, total_q, d) bytes."""
+    fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_k, d) bytes."""
     import torch
     Tq, Tk, H, d, B, p, _ = _varlen_args(
         q, k, v, ((q, "q"), (o, "o"), (do, "do"), (dq, "dq")),

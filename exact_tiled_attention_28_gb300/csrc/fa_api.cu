@@ -391,7 +391,8 @@ fa_status var_bwd(fa::Problem p, const void* q, const void* k, const void* v,
                   const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
                   void* workspace, size_t workspace_bytes, void* stream) {
   if (workspace == nullptr || !fa::aligned16(workspace) ||
-      workspace_bytes < fa::bwd_var_workspace_bytes(p.cu_q != nullptr, p.B, p.H, p.rows_q, p.d))
+      workspace_bytes <
+          fa::bwd_var_workspace_bytes(p.cu_q != nullptr, p.B, p.H, p.rows_q, p.max_k, p.d))
     return FA_ERR_WORKSPACE;
   if (!add_device(&p)) return FA_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -440,9 +441,9 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   return var_fwd(p, q, k, v, o, lse, stream);
 }
 
-size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int d) {
-  if (fa::check_sizes(B, H, total_q, d, 1.f) != FA_OK) return 0;
-  return fa::bwd_var_workspace_bytes(true, B, H, total_q, d);
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_k, int d) {
+  if (fa::check_sizes(B, H, total_q, d, 1.f) != FA_OK || max_seqlen_k < 1) return 0;
+  return fa::bwd_var_workspace_bytes(true, B, H, total_q, max_seqlen_k, d);
 }
 
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,

@@ -171,7 +171,23 @@ struct BwdVarArgs {
   float scale, scale_log2;
   Strides sdk, sdv;
   VarGeom g;
+  // packed batch: the compacted, longest-first schedule (seq.cuh, Sched) in
+  // the workspace, written by bwd_var_sched_kernel; levels = key tiles,
+  // causal visited from 0 (the most query blocks). Null for a dense batch.
+  int* sched;
+  int n_seq, sched_P;
 };
+
+// The compacted schedule of a packed batch (one block): every sequence with
+// keys owns its key tiles as levels, also when it has no queries (those items
+// zero its dK and dV).
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kSchedBuildThreads) bwd_var_sched_kernel(VarGeom g, int n_seq,
+                                                                           int P, int* base) {
+  build_sched(sched_arrays(base, n_seq, P), n_seq, P, g.H, CAUSAL, /*top_first=*/false,
+              [&](int b) { return (seq_of(b * g.H, g).nk + kTile - 1) / kTile; },
+              base + sched_ints(n_seq, P), static_cast<int>(sched_build_scratch_ints(P)));
+}
 
 template <bool VAR>
 struct BwdArgsOf {
@@ -383,10 +399,6 @@ __device__ __forceinline__ void cp_bulk_g2s(uint32_t dst, const void* src, uint3
       : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // 512 threads at 128 registers fill the register file (each SM sub-partition
 // holds one warp of every warpgroup: 4 x 32 x 128 = 16384). The warpgroups then
 // rebalance with setmaxnreg: compute 128, dQ readout 176, load/MMA 80; per
@@ -446,6 +458,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  int n_eff = a.n_items;  // items of the schedule
+  if constexpr (VAR) {
+    if (a.sched != nullptr)
+      n_eff = sched_total(sched_arrays(a.sched, a.n_seq, a.sched_P), a.n_seq, a.sched_P, CAUSAL);
+  }
 
   if (warp >= kBwdLoadWarp) {
     setmaxnreg_dec<80>();
@@ -458,9 +475,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
         const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
-        if (item >= a.n_items) break;  // only in the last, partial round
+        if (item >= n_eff) break;  // only in the last, partial round
         int bh, j;
-        decode_kv_item(item, a, CAUSAL, bh, j);
+        if constexpr (VAR) {
+          if (a.sched != nullptr) {
+            int b, h;
+            sched_decode(sched_arrays(a.sched, a.n_seq, a.sched_P), a.n_seq, a.sched_P, a.g.H,
+                         CAUSAL, false, item, b, h, j);
+            bh = b * a.g.H + h;
+          } else {
+            decode_kv_item(item, a, CAUSAL, bh, j);
+          }
+        } else {
+          decode_kv_item(item, a, CAUSAL, bh, j);
+        }
         int hh, bb, q0 = 0, k0 = 0, n_it;
         KvWork w;
         size_t lrow = 0;  // VAR: first padded D / lse2 row of the sequence
@@ -597,9 +625,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
       for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd, ++kv_round) {
         const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
-        if (item >= a.n_items) break;  // only in the last, partial round
+        if (item >= n_eff) break;  // only in the last, partial round
         int bh, j;
-        decode_kv_item(item, a, CAUSAL, bh, j);
+        if constexpr (VAR) {
+          if (a.sched != nullptr) {
+            int b, h;
+            sched_decode(sched_arrays(a.sched, a.n_seq, a.sched_P), a.n_seq, a.sched_P, a.g.H,
+                         CAUSAL, false, item, b, h, j);
+            bh = b * a.g.H + h;
+          } else {
+            decode_kv_item(item, a, CAUSAL, bh, j);
+          }
+        } else {
+          decode_kv_item(item, a, CAUSAL, bh, j);
+        }
         int n_it;
         if constexpr (VAR) {
           n_it = var_kv_work(j, seq_of(bh, a.g), CAUSAL).n_it;
@@ -689,9 +728,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t ds_row = sDS + wg * kBlk + r * 128;
     for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd, ++kv_round) {
       const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
-      if (item >= a.n_items) break;  // only in the last, partial round
+      if (item >= n_eff) break;  // only in the last, partial round
       int bh, j;
-      decode_kv_item(item, a, CAUSAL, bh, j);
+      if constexpr (VAR) {
+        if (a.sched != nullptr) {
+          int b, h;
+          sched_decode(sched_arrays(a.sched, a.n_seq, a.sched_P), a.n_seq, a.sched_P, a.g.H,
+                       CAUSAL, false, item, b, h, j);
+          bh = b * a.g.H + h;
+        } else {
+          decode_kv_item(item, a, CAUSAL, bh, j);
+        }
+      } else {
+        decode_kv_item(item, a, CAUSAL, bh, j);
+      }
       int n_it;
       KvWork w;
       int key_thr = 0;  // VAR: key row of this thread minus (nk - nq); >= 2^29 past nk
@@ -846,9 +896,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
         const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
-        if (item >= a.n_items) break;  // only in the last, partial round
+        if (item >= n_eff) break;  // only in the last, partial round
         int bh, j;
-        decode_kv_item(item, a, CAUSAL, bh, j);
+        if constexpr (VAR) {
+          if (a.sched != nullptr) {
+            int b, h;
+            sched_decode(sched_arrays(a.sched, a.n_seq, a.sched_P), a.n_seq, a.sched_P, a.g.H,
+                         CAUSAL, false, item, b, h, j);
+            bh = b * a.g.H + h;
+          } else {
+            decode_kv_item(item, a, CAUSAL, bh, j);
+          }
+        } else {
+          decode_kv_item(item, a, CAUSAL, bh, j);
+        }
         int n_it, nq_rows;
         KvWork w;
         float* acc_base;  // accumulator row 0 of this (sequence, head)
@@ -968,6 +1029,12 @@ cudaError_t launch_bwd_var_t(const Problem& p, const CUtensorMap* maps, const Pr
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  if (a.sched != nullptr) {
+    bwd_var_sched_kernel<CAUSAL><<<1, kSchedBuildThreads, 0, stream>>>(a.g, a.n_seq, a.sched_P,
+                                                                       a.sched);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   {
     constexpr int smem = bwd_smem_bytes<D>();
     auto kern = bwd_dkdv_kernel<D, CAUSAL, true>;
@@ -1026,6 +1093,13 @@ cudaError_t launch_bwd_var(const Problem& p, const void* q, const void* k, const
   a.sdk = p.st[kdK];
   a.sdv = p.st[kdV];
   a.g = g;
+  a.n_seq = p.B;
+  a.sched_P = (p.max_k + kTile - 1) / kTile;
+  // packed: the schedule's arrays after the accumulator (16-byte aligned)
+  a.sched = packed ? reinterpret_cast<int*>(
+                         ws + 2 * static_cast<size_t>(planes) * lpad +
+                         (static_cast<size_t>(planes) * p.rows_q * p.d + 3) / 4 * 4)
+                   : nullptr;
   DqArgs qa;  // the accumulator as planes x rows_q rows after 2 x planes x lpad floats
   qa.ws = Workspace{ws};
   qa.dq = static_cast<__nv_bfloat16*>(dq);
@@ -1053,10 +1127,15 @@ cudaError_t launch_bwd_var(const Problem& p, const void* q, const void* k, const
 
 }  // namespace
 
-size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int d) {
+size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int max_k, int d) {
   const size_t planes = static_cast<size_t>(packed ? 1 : B) * H;
   const size_t lpad = static_cast<size_t>(var_padded_rows(packed, B, rows_q));
-  return (2 * planes * lpad + planes * static_cast<size_t>(rows_q) * d) * 4;
+  const size_t acc = (planes * static_cast<size_t>(rows_q) * d + 3) / 4 * 4;
+  // packed: the compacted schedule's arrays after the accumulator, then the
+  // builder's scratch
+  const int P = (max_k + kTile - 1) / kTile;
+  const size_t sched = packed ? sched_ints(B, P) + sched_build_scratch_ints(P) : 0;
+  return (2 * planes * lpad + acc + sched) * 4;
 }
 
 size_t bwd_workspace_bytes(int B, int H, int N, int d) {

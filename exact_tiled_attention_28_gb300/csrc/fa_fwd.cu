@@ -106,10 +106,16 @@ struct FwdVarArgs {
   float* lse;  // [planes, rows_q] with planes = batch coordinates x H
   int* status;
   int BH, n_pairs, n_items;  // BH = sequences x heads; pairs of the longest sequence
+  int n_seq;    // sequences
+  int compact;  // packed batch: compacted schedule built in shared memory
   float scale, scale_log2;
   Strides so;
   VarGeom g;
 };
+
+// Packed batches get the compacted, longest-first schedule (seq.cuh,
+// Sched) when its arrays fit in the spare shared memory; the levels are the
+// query-tile pairs, causal visited from the highest (the most key tiles).
 
 template <bool VAR>
 struct FwdArgsOf {
@@ -152,7 +158,7 @@ __device__ __forceinline__ int var_tile_steps(int qt, const Seq& s, bool causal)
   return max(n, 1);
 }
 
-template <int D, bool CAUSAL, bool VAR>
+template <int D, bool CAUSAL, bool VAR, bool COMPACT = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const typename FwdArgsOf<VAR>::type a) {
@@ -192,6 +198,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
+  Sched sched{};          // compacted schedule of a packed batch (VAR && COMPACT)
+  int n_eff = a.n_items;  // items of the schedule
+  if constexpr (VAR && COMPACT) {
+    sched = sched_arrays(reinterpret_cast<int*>(smem + Cfg::kQBytes + Cfg::kRingBytes +
+                                                ((sizeof(FwdBarriers) + 15) / 16) * 16),
+                         a.n_seq, a.n_pairs);
+    // scratch: the K/V ring, which no copy uses before the roles start
+    build_sched(
+        sched, a.n_seq, a.n_pairs, a.g.H, CAUSAL, /*top_first=*/true,
+        [&](int b) { return (seq_of(b * a.g.H, a.g).nq + 2 * kTile - 1) / (2 * kTile); },
+        reinterpret_cast<int*>(smem + Cfg::kQBytes), Cfg::kRingBytes / 4);
+    n_eff = sched_total(sched, a.n_seq, a.n_pairs, CAUSAL);
+    fence_proxy_async_smem();  // before TMA writes into the ring
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -207,9 +227,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
         const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
-        if (item >= a.n_items) break;  // only in the last, partial round
+        if (item >= n_eff) break;  // only in the last, partial round
         int bh, pair;
-        decode_item(item, a, CAUSAL, bh, pair);
+        if constexpr (VAR && COMPACT) {
+          int b, h;
+          sched_decode(sched, a.n_seq, a.n_pairs, a.g.H, CAUSAL, true, item, b, h, pair);
+          bh = b * a.g.H + h;
+        } else {
+          decode_item(item, a, CAUSAL, bh, pair);
+        }
         int hh, bb, q0 = 0, k0 = 0, J;
         if constexpr (VAR) {
           const Seq sq = seq_of(bh, a.g);
@@ -303,9 +329,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
       for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd, ++q_round) {
         const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
-        if (item >= a.n_items) break;  // only in the last, partial round
+        if (item >= n_eff) break;  // only in the last, partial round
         int bh, pair;
-        decode_item(item, a, CAUSAL, bh, pair);
+        if constexpr (VAR && COMPACT) {
+          int b, h;
+          sched_decode(sched, a.n_seq, a.n_pairs, a.g.H, CAUSAL, true, item, b, h, pair);
+          bh = b * a.g.H + h;
+        } else {
+          decode_item(item, a, CAUSAL, bh, pair);
+        }
         int Jt[2];
         if constexpr (VAR) {
           const Seq sq = seq_of(bh, a.g);
@@ -400,9 +432,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = true;
     for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
       const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
-      if (item >= a.n_items) break;  // only in the last, partial round
+      if (item >= n_eff) break;  // only in the last, partial round
       int bh, pair;
-      decode_item(item, a, CAUSAL, bh, pair);
+      if constexpr (VAR && COMPACT) {
+        int b, h;
+        sched_decode(sched, a.n_seq, a.n_pairs, a.g.H, CAUSAL, true, item, b, h, pair);
+        bh = b * a.g.H + h;
+      } else {
+        decode_item(item, a, CAUSAL, bh, pair);
+      }
       const int qt = 2 * pair + t;
       int J;
       int key_lim = 0;  // VAR: the last key this row may see, relative to the sequence
@@ -565,12 +603,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool CAUSAL, bool VAR = false>
+template <int D, bool CAUSAL, bool VAR = false, bool COMPACT = false>
 cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const typename FwdArgsOf<VAR>::type& a,
-                         cudaStream_t stream) {
-  constexpr int smem = fwd_smem_bytes<D>();
-  auto kern = fwd_kernel<D, CAUSAL, VAR>;
+                         cudaStream_t stream, int extra_smem = 0) {
+  const int smem = fwd_smem_bytes<D>() + extra_smem;
+  auto kern = fwd_kernel<D, CAUSAL, VAR, COMPACT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = min(a.n_items, p.num_sms);
@@ -579,6 +617,17 @@ cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensor
 }
 
 }  // namespace
+
+template <int D>
+cudaError_t launch_var_d(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                         const CUtensorMap& mv, const FwdVarArgs& a, cudaStream_t stream,
+                         int extra) {
+  if (a.compact)
+    return p.causal ? launch_fwd_t<D, true, true, true>(p, mq, mk, mv, a, stream, extra)
+                    : launch_fwd_t<D, false, true, true>(p, mq, mk, mv, a, stream, extra);
+  return p.causal ? launch_fwd_t<D, true, true>(p, mq, mk, mv, a, stream)
+                  : launch_fwd_t<D, false, true>(p, mq, mk, mv, a, stream);
+}
 
 cudaError_t launch_fwd_var(const Problem& p, const void* q, const void* k, const void* v,
                            void* o, float* lse, cudaStream_t stream) {
@@ -600,19 +649,27 @@ cudaError_t launch_fwd_var(const Problem& p, const void* q, const void* k, const
   a.scale_log2 = p.scale * 1.4426950408889634f;
   a.so = p.st[kO];
   a.g = VarGeom{p.cu_q, p.cu_k, p.H, p.N, p.Nk, p.rows_q, p.rows_k, p.max_q, p.max_k};
+  a.n_seq = p.B;
+  // the schedule's arrays after the barriers (their size rounded up to 16
+  // bytes), if they fit in the shared memory the kernel leaves spare
+  const size_t sched_bytes = 16 + 4 * sched_ints(p.B, a.n_pairs);
+  const size_t base_bytes = p.d <= 32 ? fwd_smem_bytes<32>() : p.d <= 64 ? fwd_smem_bytes<64>()
+                          : p.d <= 96 ? fwd_smem_bytes<96>() : fwd_smem_bytes<128>();
+  // the builder's per-warp counters (P + 1 ints per warp, at least one warp)
+  // go into the K/V ring
+  const int ring_ints = (p.d <= 32 ? FwdCfg<32>::kRingBytes : p.d <= 64 ? FwdCfg<64>::kRingBytes
+                         : p.d <= 96 ? FwdCfg<96>::kRingBytes : FwdCfg<128>::kRingBytes) / 4;
+  a.compact = packed && base_bytes + sched_bytes <= 232448 && a.n_pairs + 1 <= ring_ints;
+  const int extra = a.compact ? static_cast<int>(sched_bytes) : 0;
   switch (p.d) {
     case 32:
-      return p.causal ? launch_fwd_t<32, true, true>(p, mq, mk, mv, a, stream)
-                      : launch_fwd_t<32, false, true>(p, mq, mk, mv, a, stream);
+      return launch_var_d<32>(p, mq, mk, mv, a, stream, extra);
     case 64:
-      return p.causal ? launch_fwd_t<64, true, true>(p, mq, mk, mv, a, stream)
-                      : launch_fwd_t<64, false, true>(p, mq, mk, mv, a, stream);
+      return launch_var_d<64>(p, mq, mk, mv, a, stream, extra);
     case 96:
-      return p.causal ? launch_fwd_t<96, true, true>(p, mq, mk, mv, a, stream)
-                      : launch_fwd_t<96, false, true>(p, mq, mk, mv, a, stream);
+      return launch_var_d<96>(p, mq, mk, mv, a, stream, extra);
     default:
-      return p.causal ? launch_fwd_t<128, true, true>(p, mq, mk, mv, a, stream)
-                      : launch_fwd_t<128, false, true>(p, mq, mk, mv, a, stream);
+      return launch_var_d<128>(p, mq, mk, mv, a, stream, extra);
   }
 }
 

@@ -90,8 +90,9 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
 // Workspace of the backward for unequal lengths (packed = false: B dense
 // sequences of rows_q query rows) or a packed batch of B sequences with
 // rows_q query rows in all: D and the log2 LSE rows (fp32) padded per
-// sequence, then the fp32 dQ accumulator.
-size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int d);
+// sequence, then the fp32 dQ accumulator (and, packed, the compacted work
+// schedule, sized by the longest key sequence max_k).
+size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int max_k, int d);
 
 // Records DEV_BADARG in the status word when the packed batch's offsets are
 // not non-decreasing from 0 to rows_q / rows_k or a length exceeds max_q /

@@ -177,13 +177,13 @@ fa_status fa_bwd_nqnk(const void* q, const void* k, const void* v, const void* o
  * device: offsets that break these rules give wrong results but no access
  * outside the buffers, and are reported as FA_ERR_INVALID_ARG by the next
  * fa_last_device_status(). fa_bwd_varlen takes a workspace of
- * fa_bwd_varlen_workspace_size(B, H, total_q, d) bytes.
+ * fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_k, d) bytes.
  */
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
                         int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
                         const long long* strides, int causal, float scale, void* stream);
-size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int d);
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_k, int d);
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,

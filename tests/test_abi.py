@@ -176,10 +176,11 @@ def test_varlen_entry_points_reject_before_launch(lib):
     assert fwd(B=1 << 20, H=1 << 11, mq=1 << 10) == fa.FA_ERR_UNSUPPORTED
     assert fwd(st=(ctypes.c_longlong * 8)(128, 256, 128, 256, 128, 256, 128, 12)) == \
         fa.FA_ERR_INVALID_ARG
-    ws = fa.fa_bwd_varlen_workspace_size(3, 2, 500, 128)
+    ws = fa.fa_bwd_varlen_workspace_size(3, 2, 500, 400, 128)
     # D and lse2 padded per sequence, plus the fp32 accumulator
     assert ws >= 4 * (2 * 2 * (512 + 128 * 4) + 2 * 500 * 128)
-    assert fa.fa_bwd_varlen_workspace_size(3, 2, 500, 48) == 0
+    assert fa.fa_bwd_varlen_workspace_size(3, 2, 500, 400, 48) == 0
+    assert fa.fa_bwd_varlen_workspace_size(3, 2, 500, 0, 128) == 0
     assert lib.fa_bwd_varlen(*([P] * 11), 3, 2, 500, 700, 300, 400, 128, None, 0, 0.1, P, ws - 1,
                              None) == fa.FA_ERR_WORKSPACE
     assert lib.fa_bwd_varlen(*([P] * 11), 3, 2, 500, 700, 300, 400, 128, None, 0, 0.1, None, ws,

@@ -29,7 +29,9 @@ def _f64(bits):
 def _check_fwd(o, lse, o_want, lse_want, what):
     """O/LSE parity; rows whose reference LSE is -inf must be O = 0, LSE = -inf."""
     empty = np.isneginf(lse_want)
-    assert np.array_equal(np.isneginf(lse), empty), f"{what}: rows without keys differ"
+    bad = np.argwhere(np.isneginf(lse) != empty)
+    assert bad.size == 0, (f"{what}: rows without keys differ at {bad[:5].tolist()} "
+                           f"(got {lse[tuple(bad[0])]}, want {lse_want[tuple(bad[0])]})")
     assert np.all(o[empty] == 0.0), f"{what}: O of a row without keys is not 0"
     if np.any(~empty):
         gu.check_o_lse(o[~empty], lse[~empty], o_want[~empty], lse_want[~empty], what)
@@ -114,7 +116,12 @@ def _varlen(fa, seed, lens_q, lens_k, H, d, causal, scale=None, views=None, max_
     lse = torch.full((H, Tq), float("nan"), dtype=torch.float32, device="cuda")
     fa.fa_fwd_varlen(dev["q"], dev["k"], dev["v"], o, lse, cq, ck, mq, mk, causal, scale)
     assert fa.fa_last_device_status() == fa.FA_OK
-    ws = torch.full((fa.fa_bwd_varlen_workspace_size(len(lens_q), H, Tq, d),), 0xFF,
+    what = f"lens_q={lens_q} lens_k={lens_k} H={H} d={d} causal={causal}"
+    o_want, lse_want = oracle.varlen_forward(x["q"], x["k"], x["v"], cu_q, cu_k, causal, scale)
+    # the forward on its own, before the backward touches anything
+    # (LSE is [H, T] while O is [T, H, d]: compare per (row, head))
+    _check_fwd(gu.to_f64(o), gu.to_f64(lse).T, o_want, lse_want.T, "forward: " + what[-60:])
+    ws = torch.full((fa.fa_bwd_varlen_workspace_size(len(lens_q), H, Tq, mk, d),), 0xFF,
                     dtype=torch.uint8, device="cuda")
     dq = torch.full_like(dev["q"], float("nan"))
     dk = torch.full_like(dev["k"], float("nan"))
@@ -122,10 +129,8 @@ def _varlen(fa, seed, lens_q, lens_k, H, d, causal, scale=None, views=None, max_
     fa.fa_bwd_varlen(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], dq, dk, dv, cq, ck, mq, mk,
                      causal, scale, ws)
     assert fa.fa_last_device_status() == fa.FA_OK
-    what = f"lens_q={lens_q} lens_k={lens_k} H={H} d={d} causal={causal}"
-    o_want, lse_want = oracle.varlen_forward(x["q"], x["k"], x["v"], cu_q, cu_k, causal, scale)
-    # LSE is [H, T] while O is [T, H, d]: compare per (row, head)
-    _check_fwd(gu.to_f64(o), gu.to_f64(lse).T, o_want, lse_want.T, what)
+    # the backward leaves the forward's outputs alone
+    _check_fwd(gu.to_f64(o), gu.to_f64(lse).T, o_want, lse_want.T, "after backward: " + what[-60:])
     want = oracle.varlen_backward(x["q"], x["k"], x["v"], x["do"], cu_q, cu_k, causal, scale)
     gu.check_grads([gu.to_f64(t) for t in (dq, dk, dv)], want, what)
     return o, lse
@@ -216,3 +221,28 @@ def test_varlen_malformed_offsets_are_reported(cuda_lib):
     assert fa.fa_last_device_status() == fa.FA_ERR_INVALID_ARG
     fa.fa_fwd_varlen(dev["q"], dev["k"], dev["v"], o, lse, cq, ck, 200, 150, True, 0.1)
     assert fa.fa_last_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("n_seq,d", [(700, 64), (5000, 64), (5000, 128)])
+def test_varlen_many_short_sequences(cuda_lib, n_seq, d):
+    """Many short sequences, some empty, most in one level class of the
+    compacted schedule, which every CTA of the forward builds for itself (at
+    d = 64 both sizes fit in its shared memory; at d = 128 the 5000 do not and
+    the forward takes the uncompacted order; the backward always builds its
+    schedule once, in the workspace). A second forward gives the same bits."""
+    import torch
+    rng = np.random.default_rng(406 + n_seq)
+    lens_q = [int(x) for x in rng.integers(0, 40, size=n_seq)]
+    lens_k = [int(x) for x in rng.integers(0, 40, size=n_seq)]
+    lens_k[0] = max(lens_k[0], 1)
+    for causal in (False, True):
+        o, lse = _varlen(cuda_lib, 406, lens_q, lens_k, 1, d, causal)
+        bits, cu_q, cu_k = inputs.packed_inputs(406, lens_q, lens_k, 1, d)
+        dev = _to_dev(bits)
+        cq = torch.tensor(cu_q, dtype=torch.int32, device="cuda")
+        ck = torch.tensor(cu_k, dtype=torch.int32, device="cuda")
+        o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+        cuda_lib.fa_fwd_varlen(dev["q"], dev["k"], dev["v"], o2, lse2, cq, ck, max(lens_q),
+                               max(lens_k), causal, gu.default_scale(d))
+        assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
