@@ -43,9 +43,9 @@ for _d, _H in ((64, 32), (128, 16)):
 # the other supported head dims, same token count (hidden 2048 at d = 32)
 WORKLOADS["dim_d32_n4096"] = (4, 64, 4096, 32)
 WORKLOADS["dim_d96_n4096"] = (4, 16, 4096, 96)
-# head dim 256 has a forward only: its step is one fa_fwd (FWD_ONLY_METRIC)
+# head dim 256 runs its own forward and dK/dV kernels (fwd256_kernel,
+# bwd256_dkdv_kernel)
 WORKLOADS["dim_d256_n4096"] = (4, 8, 4096, 256)
-FWD_ONLY_METRIC = "attention TFLOP/s fwd (bf16, 1 GB300)"
 DEFAULT_WORKLOAD = "gpt_d128_n4096"
 
 # Packed batches of variable-length sequences (fa_fwd_varlen / fa_bwd_varlen):
@@ -80,8 +80,9 @@ def varlen_lengths(name):
 # from an ncu capture of the current kernel source (see profiles/), keyed by
 # workload and causal flag; None where no capture of the current kernel exists.
 # Algorithmic bytes for comparison: q, k, v, dO read and dk, dv written once
-# (6 x 64 MiB) plus the fp32 dQ accumulator (128 MiB) = 537 MB at this size.
-NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.191e8}
+# (6 x 64 MiB) plus the fp32 dQ accumulator (128 MiB) = 537 MB at either size.
+NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.191e8,
+                           ("dim_d256_n4096", False): 6.723e8}
 
 
 def fwd_flops(B, H, N, d, causal):
@@ -249,30 +250,6 @@ def run_reference(args):
                 "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
-        return
-    if args.workload in WORKLOADS and WORKLOADS[args.workload][3] == 256:
-        import oracle
-        from exact_tiled_attention_28_gb300 import inputs
-        B, H, N, d = WORKLOADS[args.workload]
-        scale = 1.0 / math.sqrt(d)
-        xh = inputs.head_inputs_f64(1000, 0, 0, N, d, ("q", "k", "v"))
-        for _ in range(args.warmup):
-            oracle.head_forward(xh["q"], xh["k"], xh["v"], args.causal, scale)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):  # each step: the first head, forward only
-            oracle.head_forward(xh["q"], xh["k"], xh["v"], args.causal, scale)
-        dt = time.perf_counter() - t0
-        value = args.steps * fwd_flops(1, 1, N, d, args.causal) / dt / 1e12
-        print(json.dumps({
-            "impl": "reference", "metric": FWD_ONLY_METRIC, "value": value, "unit": "TFLOP/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(args, B, H, N, d),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
-                             "kind": "oracle", "sample": f"one head (N={N}, d={d}) forward per step"},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}), flush=True)
         return
     lengths = None
     if args.workload in VARLEN_WORKLOADS:
@@ -675,127 +652,6 @@ def run_decode(args):
         torch.distributed.destroy_process_group()
 
 
-def run_fwd_only(args):
-    """Workloads without a backward (d = 256): one step = one fa_fwd call."""
-    import torch
-
-    import exact_tiled_attention_28_gb300 as fa
-    from exact_tiled_attention_28_gb300 import inputs, replicas
-
-    world, rank, local = dist_setup(args)
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    fa.load()
-    dev = torch.device("cuda", torch.cuda.current_device())
-    B, H, N, d = WORKLOADS[args.workload]
-    causal = bool(args.causal)
-    scale = 1.0 / math.sqrt(d)
-    seed = replicas.replica_seed(1000, rank)
-    bits = inputs.attention_inputs(seed, B, H, N, d, ("q", "k", "v"))
-    host = {n: inputs.bits_to_torch_bf16(b).pin_memory() for n, b in bits.items()}
-    x = {n: t.to(dev) for n, t in host.items()}
-    o = torch.empty_like(x["q"])
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step():
-        fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, causal, scale)
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    if fa.fa_last_device_status() != fa.FA_OK:
-        raise RuntimeError("device status reports an error during warm-up")
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    sampler = ClockSampler(uuid)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler.start()
-    time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for _ in range(args.steps):
-        step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop()
-    if fa.fa_last_device_status() != fa.FA_OK:
-        raise RuntimeError("device status reports an error in the timed region")
-    ms_step = t_start.elapsed_time(t_end) / args.steps
-    ms_step_max = replicas.max_over_ranks(ms_step, dev)
-    # end to end: q, k, v in from pinned host memory, o and lse back, per step
-    o_host = torch.empty_like(o, device="cpu").pin_memory()
-    l_host = torch.empty_like(lse, device="cpu").pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_e2e = max(args.e2e_steps, 1)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(n_e2e):
-        for n in x:
-            x[n].copy_(host[n], non_blocking=True)
-        step()
-        o_host.copy_(o, non_blocking=True)
-        l_host.copy_(lse, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    F = fwd_flops(B, H, N, d, causal)
-    peaks = load_peaks()
-    tf = F / (ms_step * 1e-3) / 1e12
-    line = {
-        "metric": FWD_ONLY_METRIC, "value": replicas.aggregate_throughput(F, world, ms_step_max),
-        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
-        "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: Q, K, V i.i.d. N(0,1) rounded to bf16, seeded",
-        "config": {**config_of(args, B, H, N, d),
-                   "workload": f"{args.workload}: B={B} H={H} N={N} d={d} "
-                               f"{'causal' if causal else 'non-causal'} forward only"},
-        "roofline": {"kernel": "fwd256_kernel" if d == 256 else "fwd_kernel", "bound": "tensor",
-                     "achieved": tf, "peak": peaks["sustained"], "unit": "TFLOP/s",
-                     "frac": tf / peaks["sustained"],
-                     "peak_kind": f"sustained bf16 of {peaks['source']}", "traffic": None,
-                     "algorithmic": f"4*B*H*N^2*d{' / 2' if causal else ''} = {F:.4g} FLOP per launch"},
-        "e2e": {"value": F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": sum(t.numel() * 2 for t in host.values()),
-                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
-                "note": "sequential copies on the compute stream"},
-        "gpu_launches": args.steps,
-        "clocks": clocks,
-    }
-    if world > 1:
-        torch.distributed.barrier()
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-        t0 = time.perf_counter()
-        heads = 0
-        while heads == 0 or (time.perf_counter() - t0 < args.cpu_budget_s and heads < 64):
-            b, h = divmod(heads % (B * H), H)
-            xh = inputs.head_inputs_f64(seed, b, h, N, d, ("q", "k", "v"))
-            oracle.head_forward(xh["q"], xh["k"], xh["v"], causal, scale)
-            heads += 1
-        spent = time.perf_counter() - t0
-        line["cpu_baseline"] = {"value": heads * fwd_flops(1, 1, N, d, causal) / spent / 1e12,
-                                "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": f"{heads} whole heads (N={N}, d={d}) forward, "
-                                          f"{spent:.1f} s (including input generation)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
-
-
 def run_ours(args):
     import torch
 
@@ -918,13 +774,15 @@ def run_ours(args):
                     "frac_of_sustained_peak": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peaks["sustained"]},
         "bwd": {"ms": bwd_ms, "pre_ms": pre_ms, "dkdv_ms": dkdv_ms, "dq_ms": dq_ms,
                 "tflops": 2.5 * F / (bwd_ms * 1e-3) / 1e12},
-        "roofline": {"kernel": "bwd_dkdv_kernel" if args.layout == "bhnd" else "fa_bwd (all stages)",
+        "roofline": {"kernel": (("bwd256_dkdv_kernel" if d == 256 else "bwd_dkdv_kernel")
+                                if args.layout == "bhnd" else "fa_bwd (all stages)"),
                      "bound": "tensor", "achieved": dkdv_tf,
                      "peak": peaks["sustained"], "unit": "TFLOP/s",
                      "frac": dkdv_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}",
                      "traffic": traffic,
                      "algorithmic": f"2.5 x 4*B*H*N^2*d{' / 2' if causal else ''} = {2.5 * F:.4g} FLOP per launch"},
-        "roofline_fwd": {"kernel": "fwd_kernel", "bound": "tensor", "achieved": fwd_tf,
+        "roofline_fwd": {"kernel": "fwd256_kernel" if d == 256 else "fwd_kernel",
+                         "bound": "tensor", "achieved": fwd_tf,
                          "peak": peaks["sustained"], "unit": "TFLOP/s",
                          "frac": fwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}"},
         "e2e": {"value": 3.5 * F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
@@ -956,8 +814,6 @@ def main():
         run_varlen(args)
     elif args.workload in DECODE_WORKLOADS:
         run_decode(args)
-    elif WORKLOADS[args.workload][3] == 256:
-        run_fwd_only(args)
     else:
         run_ours(args)
 

@@ -65,15 +65,16 @@ cudaError_t device_info(DeviceInfo* out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// allow256: the forward of dense (or strided) equal-length batches also takes
-// d = 256; nothing else does.
+// allow256: the forward and backward of dense (or strided) equal-length
+// batches also take d = 256; nothing else does. Their work items (query
+// tiles in the forward, 64-key blocks in the backward) are counted in int.
 fa_status check_sizes(int B, int H, int N, int d, float scale, bool allow256 = false) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * H >= (int64_t(1) << 31)) return FA_ERR_UNSUPPORTED;
   if (d != 32 && d != 64 && d != 96 && d != 128 && !(allow256 && d == 256))
     return FA_ERR_UNSUPPORTED;
   if (allow256 && d == 256 &&
-      static_cast<int64_t>(B) * H * ((N + kTile - 1) / kTile) >= (int64_t(1) << 31))
+      static_cast<int64_t>(B) * H * ((static_cast<int64_t>(N) + 63) / 64) >= (int64_t(1) << 31))
     return FA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   return FA_OK;
@@ -153,14 +154,14 @@ cudaError_t launch_varlen_check(const Problem& p, cudaStream_t stream) {
 }
 
 bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
-                   const Strides& s) {
+                   const Strides& s, int box_rows) {
   if (!g_encode) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.row) * 2,
                                  static_cast<cuuint64_t>(s.head) * 2,
                                  static_cast<cuuint64_t>(s.batch) * 2};
-  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTile), 1, 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -228,7 +229,7 @@ fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, f
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
-  if (fa::check_sizes(B, H, N, d, 1.f) != FA_OK) return 0;
+  if (fa::check_sizes(B, H, N, d, 1.f, /*allow256=*/true) != FA_OK) return 0;
   return fa::bwd_workspace_bytes(B, H, N, d);
 }
 
@@ -239,7 +240,7 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
                      int causal, float scale, void* workspace, size_t workspace_bytes, int stages,
                      std::initializer_list<const void*> used, void* stream,
                      const long long* strides = nullptr) {
-  fa_status s = fa::check_sizes(B, H, N, d, scale);
+  fa_status s = fa::check_sizes(B, H, N, d, scale, /*allow256=*/true);
   if (s != FA_OK) return s;
   s = fa::check_ptrs(used);
   if (s != FA_OK) return s;

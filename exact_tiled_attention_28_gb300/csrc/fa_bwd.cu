@@ -104,13 +104,14 @@ static_assert(bwd_smem_bytes<96>() <= 232448, "backward shared memory over the s
 
 // The workspace: D and the lse rows in log2 units, each fp32 [BH, Npad], then
 // the fp32 dQ accumulator [BH, N, d].
+// (Host code reads the same offsets to hand them to the d = 256 kernel.)
 struct Workspace {
   float* base;
-  __device__ __forceinline__ float* Drow(int BH, int Npad) const { return base; }
-  __device__ __forceinline__ float* lse2(int BH, int Npad) const {
+  __host__ __device__ __forceinline__ float* Drow(int BH, int Npad) const { return base; }
+  __host__ __device__ __forceinline__ float* lse2(int BH, int Npad) const {
     return base + static_cast<size_t>(BH) * Npad;
   }
-  __device__ __forceinline__ float* dq_acc(int BH, int Npad) const {
+  __host__ __device__ __forceinline__ float* dq_acc(int BH, int Npad) const {
     return base + 2 * static_cast<size_t>(BH) * Npad;
   }
 };
@@ -210,7 +211,7 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
   // each active lane handles 8 elements (16 bytes) of a row; rows take a
   // power-of-two number of lanes, the ones past d / 8 idle (d = 96)
-  constexpr int kLanesPerRow = D <= 32 ? 4 : (D <= 64 ? 8 : 16);
+  constexpr int kLanesPerRow = D <= 32 ? 4 : (D <= 64 ? 8 : (D <= 128 ? 16 : 32));
   constexpr int kActive = D / 8;
   const size_t rows = static_cast<size_t>(a.BH) * a.Npad;
   float* const Drow = a.ws.Drow(a.BH, a.Npad);
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
 // so that its P is 0 and it adds nothing to any gradient.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_var_kernel(const PreVarArgs a) {
-  constexpr int kLanesPerRow = D <= 32 ? 4 : (D <= 64 ? 8 : 16);
+  constexpr int kLanesPerRow = D <= 32 ? 4 : (D <= 64 ? 8 : (D <= 128 ? 16 : 32));
   constexpr int kActive = D / 8;
   const size_t units = static_cast<size_t>(a.BH) * a.max_q_pad;
   float* const Drow = a.ws;
@@ -388,15 +389,6 @@ __device__ __forceinline__ int var_qblock(const KvWork& w, int u, bool causal) {
   if (causal) return w.i0 + u;
   const int i = w.rot + u;
   return i < w.n_q ? i : i - w.n_q;
-}
-
-__device__ __forceinline__ void cp_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
 }
 
 // 512 threads at 128 registers fill the register file (each SM sub-partition
@@ -994,21 +986,44 @@ template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const PreArgs& pa,
                          const BwdArgs& a, const DqArgs& qa, int stages, cudaStream_t stream) {
   if (stages & kStagePre) {
-    const size_t work = static_cast<size_t>(a.BH) * a.Npad * (D <= 32 ? 4 : (D <= 64 ? 8 : 16));
+    const size_t work = static_cast<size_t>(a.BH) * a.Npad * (D <= 32 ? 4 : (D <= 64 ? 8 : (D <= 128 ? 16 : 32)));
     const int grid = static_cast<int>(std::min<size_t>((work + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
     bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(pa);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (stages & kStageDkdv) {
-    constexpr int smem = bwd_smem_bytes<D>();
-    auto kern = bwd_dkdv_kernel<D, CAUSAL, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const int grid = min(a.n_items, p.num_sms);
-    kern<<<grid, kBwdThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if constexpr (D == 256) {  // its own kernel over 64-key blocks (fa_bwd256.cu)
+      Bwd256Args b;
+      b.lse2 = a.ws.lse2(a.BH, a.Npad);
+      b.Drow = a.ws.Drow(a.BH, a.Npad);
+      b.dq_acc = a.ws.dq_acc(a.BH, a.Npad);
+      b.dk = a.dk;
+      b.dv = a.dv;
+      b.status = a.status;
+      b.N = a.N;
+      b.H = a.H;
+      b.Npad = a.Npad;
+      b.BH = a.BH;
+      b.n_kb = (a.N + 63) / 64;
+      b.n_qb = a.n_tiles;
+      b.n_items = a.BH * b.n_kb;
+      b.scale = a.scale;
+      b.scale_log2 = a.scale_log2;
+      b.sdk = a.sdk;
+      b.sdv = a.sdv;
+      const cudaError_t e = launch_bwd256_dkdv(p, maps[0], maps[1], maps[2], maps[3], b, stream);
+      if (e != cudaSuccess) return e;
+    } else {
+      constexpr int smem = bwd_smem_bytes<D>();
+      auto kern = bwd_dkdv_kernel<D, CAUSAL, false>;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      const int grid = min(a.n_items, p.num_sms);
+      kern<<<grid, kBwdThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], a);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   if (stages & kStageDq) {
     const size_t n8 = static_cast<size_t>(a.BH) * a.N * D / 8;
@@ -1023,7 +1038,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_bwd_var_t(const Problem& p, const CUtensorMap* maps, const PreVarArgs& pa,
                              const BwdVarArgs& a, const DqArgs& qa, cudaStream_t stream) {
   {
-    const size_t work = static_cast<size_t>(pa.BH) * pa.max_q_pad * (D <= 32 ? 4 : (D <= 64 ? 8 : 16));
+    const size_t work = static_cast<size_t>(pa.BH) * pa.max_q_pad * (D <= 32 ? 4 : (D <= 64 ? 8 : (D <= 128 ? 16 : 32)));
     const int grid = static_cast<int>(std::min<size_t>((work + 255) / 256, static_cast<size_t>(p.num_sms) * 8));
     bwd_pre_var_kernel<D><<<grid, 256, 0, stream>>>(pa);
     const cudaError_t e = cudaGetLastError();
@@ -1153,10 +1168,12 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
   }
   const int BH = p.B * p.H;
   CUtensorMap maps[4];
-  if ((stages & kStageDkdv) && (!make_tile_map(&maps[0], q, p.B, p.H, p.N, p.d, p.st[kQ]) ||
-                                 !make_tile_map(&maps[1], k, p.B, p.H, p.N, p.d, p.st[kK]) ||
-                                 !make_tile_map(&maps[2], v, p.B, p.H, p.N, p.d, p.st[kV]) ||
-                                 !make_tile_map(&maps[3], dO, p.B, p.H, p.N, p.d, p.st[kdO])))
+  const int kv_rows = p.d == 256 ? 64 : kTile;  // the d = 256 kernel takes 64-key blocks
+  if ((stages & kStageDkdv) &&
+      (!make_tile_map(&maps[0], q, p.B, p.H, p.N, p.d, p.st[kQ]) ||
+       !make_tile_map(&maps[1], k, p.B, p.H, p.N, p.d, p.st[kK], kv_rows) ||
+       !make_tile_map(&maps[2], v, p.B, p.H, p.N, p.d, p.st[kV], kv_rows) ||
+       !make_tile_map(&maps[3], dO, p.B, p.H, p.N, p.d, p.st[kdO])))
     return cudaErrorInvalidValue;
   const int n_tiles = (p.N + kTile - 1) / kTile;
   const Workspace ws{static_cast<float*>(workspace)};
@@ -1205,6 +1222,9 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
     case 96:
       return p.causal ? launch_bwd_t<96, true>(p, maps, pa, a, qa, stages, stream)
                       : launch_bwd_t<96, false>(p, maps, pa, a, qa, stages, stream);
+    case 256:
+      return p.causal ? launch_bwd_t<256, true>(p, maps, pa, a, qa, stages, stream)
+                      : launch_bwd_t<256, false>(p, maps, pa, a, qa, stages, stream);
     default:
       return p.causal ? launch_bwd_t<128, true>(p, maps, pa, a, qa, stages, stream)
                       : launch_bwd_t<128, false>(p, maps, pa, a, qa, stages, stream);

@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace fa {
@@ -47,11 +48,32 @@ inline Strides contiguous_strides(int H, int N, int d) {
 }
 
 // Encodes a 4-D TMA map (d, N, H, B) over a bf16 tensor with the given
-// strides, a {64, 128, 1, 1} box and 128-byte swizzle. Returns false on failure.
+// strides, a {64, box_rows, 1, 1} box and 128-byte swizzle. Returns false on
+// failure.
 bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
-                   const Strides& s);
+                   const Strides& s, int box_rows = kTile);
 
 // Launchers; they return a cudaError_t from the launch.
+
+// The dK / dV stage at head dimension 256 (fa_bwd256.cu): its own kernel over
+// 64-key blocks. The workspace rows are those of the d <= 128 backward:
+// lse2 and D fp32 [BH, Npad] (Npad = N rounded up to 128; pad rows lse2 =
+// +inf, D = 0) and the fp32 dQ accumulator [BH, N, 256].
+struct Bwd256Args {
+  const float* lse2;
+  const float* Drow;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  int N, H, Npad, BH, n_kb, n_qb, n_items;
+  float scale, scale_log2;
+  Strides sdk, sdv;
+};
+// maps: q and dO with 128-row boxes, k and v with 64-row boxes.
+cudaError_t launch_bwd256_dkdv(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                               const CUtensorMap& mv, const CUtensorMap& mdo,
+                               const Bwd256Args& a, cudaStream_t stream);
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream);
 

@@ -23,10 +23,12 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
  *    aligned. The library keeps no reference to them after the call.
  *  - d must be 32, 64, 96 or 128; B, H, N >= 1; B*H < 2^31 (offsets are computed in
- *    64 bits, so a tensor may hold more than 2^31 elements). fa_fwd and
- *    fa_fwd_strided also take d = 256 ("Flash Attention v2" notes,
- *    "Detailed Differences", 3 "Head Dimension Support"); no other entry
- *    point does (FA_ERR_UNSUPPORTED).
+ *    64 bits, so a tensor may hold more than 2^31 elements). The dense
+ *    entry points also take d = 256 ("Flash Attention v2" notes, "Detailed
+ *    Differences", 3 "Head Dimension Support"): fa_fwd, fa_fwd_strided,
+ *    fa_bwd, fa_bwd_strided, fa_bwd_workspace_size, the three backward
+ *    stages and fa_bwd_noalloc, with B*H*ceil(N/64) < 2^31. The unequal-
+ *    length, packed and decode entry points reject it (FA_ERR_UNSUPPORTED).
  *  - Causal masking is top-left aligned with equal query and key lengths:
  *    query i sees keys j <= i. scale must be finite and >= 0.
  *  - stream is a cudaStream_t (NULL = the legacy default stream). Every call

@@ -91,7 +91,7 @@ def test_bwd_rejects_before_launch(lib):
     for i in range(9):
         assert bwd(lib, null=i) == fa.FA_ERR_INVALID_ARG
     assert bwd(lib, d=48) == fa.FA_ERR_UNSUPPORTED
-    assert bwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED  # d = 256 has a forward only
+    assert bwd(lib, d=512) == fa.FA_ERR_UNSUPPORTED
     assert bwd(lib, ws=None) == fa.FA_ERR_WORKSPACE
     assert bwd(lib, ws=P + 4) == fa.FA_ERR_WORKSPACE
     assert bwd(lib, ws_bytes=fa.fa_bwd_workspace_size(1, 1, 128, 64) - 1) == fa.FA_ERR_WORKSPACE
@@ -203,13 +203,22 @@ def test_decode_rejects_before_launch(lib):
     assert fa.fa_decode_workspace_size(1, 1, 17, 1000, 128) == 0
 
 
-def test_d256_is_forward_only(lib):
-    """d = 256 passes the forward's argument checks (on a host without a GPU
-    the call then fails at the device query, not as unsupported); every other
-    entry point rejects it."""
+def test_d256_dense_forward_and_backward_only(lib):
+    """d = 256 passes the dense forward's and backward's argument checks (on a
+    host without a GPU the call then fails at the device query, not as
+    unsupported); the unequal-length, packed and decode entry points reject
+    it."""
     assert fwd(lib, d=256) != fa.FA_ERR_UNSUPPORTED
     assert fwd(lib, d=256, q=None) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_bwd_workspace_size(1, 1, 128, 256) == 0
+    ws = fa.fa_bwd_workspace_size(1, 1, 128, 256)
+    # D and lse2 rows (2 x 128 fp32) and the fp32 dQ accumulator (128 x 256)
+    assert ws == (2 * 128 + 128 * 256) * 4
+    assert bwd(lib, d=256, ws_bytes=ws) != fa.FA_ERR_UNSUPPORTED
+    assert bwd(lib, d=256, ws_bytes=ws) != fa.FA_ERR_INVALID_ARG
+    assert bwd(lib, d=256, ws_bytes=ws - 1) == fa.FA_ERR_WORKSPACE
+    assert bwd(lib, d=256, null=3, ws_bytes=ws) == fa.FA_ERR_INVALID_ARG
+    # 64-key work items are counted in int
+    assert fa.fa_bwd_workspace_size(1 << 15, 1 << 10, 1 << 12, 256) == 0
     assert lib.fa_fwd_nqnk(P, P, P, P, P, 1, 1, 10, 20, 256, None, 0, 0.1, None) == \
         fa.FA_ERR_UNSUPPORTED
     assert lib.fa_decode(P, P, P, P, P, None, 1, 1, 1, 100, 256, None, 0, 0.1, None, 0, None) == \

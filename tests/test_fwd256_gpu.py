@@ -1,6 +1,6 @@
 """Forward parity at head dimension 256 (its own kernel: one query tile per
 CTA with a double-buffered S in TMEM) through the C ABI against the fp64
-oracle. d = 256 has no backward; fa_bwd rejects it."""
+oracle. The backward at d = 256 is covered in test_bwd256_gpu.py."""
 
 import numpy as np
 import pytest
@@ -62,15 +62,3 @@ def test_d256_full_size_sampled(cuda_lib, causal):
         x = gu.head_f64(bits, b, h, ("q", "k", "v"))
         ow, lw = oracle.head_forward(x["q"], x["k"], x["v"], causal, scale, rows=rows)
         gu.check_o_lse(og[b, h, rows], lg[b, h, rows], ow, lw, f"b={b} h={h}")
-
-
-def test_d256_backward_is_rejected(cuda_lib):
-    import torch
-    fa = cuda_lib
-    B, H, N, d = 1, 1, 128, 256
-    x = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
-    lse = torch.zeros((B, H, N), dtype=torch.float32, device="cuda")
-    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
-    with pytest.raises(fa.FaError) as e:
-        fa.fa_bwd(x, x, x, x, lse, x, x.clone(), x.clone(), x.clone(), False, 0.1, ws)
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED
