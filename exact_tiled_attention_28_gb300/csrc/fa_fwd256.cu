@@ -13,10 +13,9 @@
 //
 // Shared memory: Q (128 x 256 bf16, 64 KiB) and a ring of five 32 KiB
 // half-tiles (128 rows x 128 columns: two 64-column blocks) through which K
-// and V stream in the order K(j) cols 0-127, K(j) cols 128-255, V(j) cols
-// 0-127, V(j) cols 128-255. S(j) consumes K(j) before PV(j-1) consumes
-// V(j-1); five slots keep the loader a half-tile ahead of that order. PV runs
-// as two N = 128 MMAs per 16-key step, one per V half.
+// and V stream, each tile as its columns 0-127 then 128-255, in the order the
+// MMAs use them: K(0), K(1), V(0), K(2), V(1), ... (kv_load). PV runs as two
+// N = 128 MMAs per 16-key step, one per V half.
 //
 // 192 threads: warps 0-3 softmax (one thread per query row = TMEM lane),
 // warp 4 TMA loader, warp 5 MMA issuer. Persistent, one CTA per SM, one
@@ -79,6 +78,17 @@ __device__ __forceinline__ void decode256(int item, const Fwd256Args& a, bool ca
     bh = item / a.n_tiles;
     qt = item % a.n_tiles;
   }
+}
+
+// Position of K(j) (or V(j)) among an item's half-tile loads. The MMAs use
+// the tiles in the order K(0), K(1), V(0), K(2), V(1), ..., K(J - 1),
+// V(J - 2), V(J - 1) (S(j + 1) is issued before PV(j)), and the loader
+// issues them in that order, two half-tiles each. Loading K(j + 1) after V(j)
+// instead would start K(j + 2) only once PV(j) has freed ring slots, right
+// when S(j + 2) needs it: a full load latency per tile.
+__device__ __forceinline__ uint32_t kv_load(bool v, int j, int J) {
+  if (!v) return j == 0 ? 0u : 4u * j - 2u;
+  return j == J - 1 ? 4u * J - 2u : 4u * j + 4u;
 }
 
 template <bool CAUSAL>
@@ -148,18 +158,23 @@ __global__ void __launch_bounds__(kThreads256, 1)
           for (int cb = 0; cb < 4; ++cb)
             tma_load_4d(sQ + cb * kBlk, &tmQ, bar, 64 * cb, qt * kTile, hh, bb, pol_q);
         }
-        for (int j = 0; j < J && ok; ++j) {
-          for (int w = 0; w < 4; ++w, ++n) {  // K cols 0-127, K 128-255, V 0-127, V 128-255
+        // tiles in the order the MMAs consume them: K(0), then K(j), V(j - 1)
+        // for j = 1 .. J - 1, then V(J - 1) (see kv_load)
+        for (int t = 0; t < 2 * J && ok; ++t) {
+          const bool is_v = t > 0 && (t == 2 * J - 1 || (t & 1) == 0);
+          const int tile = is_v ? (t == 2 * J - 1 ? J - 1 : t / 2 - 1) : (t + 1) / 2;
+          for (int w = 0; w < 2; ++w, ++n) {  // columns 0-127, then 128-255
             const uint32_t s = n % kSlots;
             ok = mbar_wait(smem_u32(&bars->kv_empty[s]), ((n / kSlots) & 1) ^ 1, abort,
                            a.status);
             if (!ok) break;
             const uint32_t bar = smem_u32(&bars->kv_full[s]);
-            const CUtensorMap* map = w < 2 ? &tmK : &tmV;
-            const int c0 = 128 * (w & 1);
+            const CUtensorMap* map = is_v ? &tmV : &tmK;
+            const int c0 = 128 * w;
             mbar_arrive_expect_tx(bar, kHalfBytes);
-            tma_load_4d(sRing + s * kHalfBytes, map, bar, c0, j * kTile, hh, bb, pol_kv);
-            tma_load_4d(sRing + s * kHalfBytes + kBlk, map, bar, c0 + 64, j * kTile, hh, bb, pol_kv);
+            tma_load_4d(sRing + s * kHalfBytes, map, bar, c0, tile * kTile, hh, bb, pol_kv);
+            tma_load_4d(sRing + s * kHalfBytes + kBlk, map, bar, c0 + 64, tile * kTile, hh, bb,
+                        pol_kv);
           }
         }
       }
@@ -218,7 +233,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         tc_fence_after();
         for (int j = 0; j <= J && ok; ++j) {
           if (j < J) {  // S(j)
-            const uint32_t nk0 = n + 4 * j, nk1 = nk0 + 1;
+            const uint32_t nk0 = n + kv_load(false, j, J), nk1 = nk0 + 1;
             const uint32_t s0 = nk0 % kSlots, s1 = nk1 % kSlots;
             ok = mbar_wait(smem_u32(&bars->kv_full[s0]), (nk0 / kSlots) & 1, abort, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bars->kv_full[s1]), (nk1 / kSlots) & 1, abort, a.status);
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
             }
             ok = mbar_wait(smem_u32(&bars->p_full[g & 1]), (g >> 1) & 1, abort, a.status);
             if (!ok) break;
-            const uint32_t nv0 = n + 4 * (j - 1) + 2, nv1 = nv0 + 1;
+            const uint32_t nv0 = n + kv_load(true, j - 1, J), nv1 = nv0 + 1;
             const uint32_t s0 = nv0 % kSlots, s1 = nv1 % kSlots;
             ok = mbar_wait(smem_u32(&bars->kv_full[s0]), (nv0 / kSlots) & 1, abort, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bars->kv_full[s1]), (nv1 / kSlots) & 1, abort, a.status);
