@@ -25,9 +25,9 @@
 // Shared memory (224 KiB + rows): Q_i and dO_i (128 x 256 bf16 each), K_j and
 // V_j (64 x 256 each), P and dS (128 x 64 each, written by the compute warps
 // in the 128-byte swizzled layout the MMAs read), the lse2 and D rows of
-// block i. There is room for one Q_i / dO_i buffer only: dO_i is released
-// after the dV MMAs and Q_i after the dK MMAs, so the next block's copies
-// overlap the dQ^T MMAs.
+// block i. There is room for one Q_i / dO_i buffer only. The dK MMAs run
+// first and release Q_i, whose successor the next block's S needs first; dO_i
+// follows after the dV MMAs; both copies overlap the dQ^T MMAs.
 //
 // 384 threads: warp 0 TMA loader, warp 1 MMA issuer, warps 4-7 compute (one
 // thread per query row = TMEM lane), warps 8-11 dQ^T read-out and the dK /
@@ -173,28 +173,29 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         for (int i = i0; i < a.n_qb && ok; ++i, ++g) {
           const size_t row0 = static_cast<size_t>(bh) * a.Npad + static_cast<size_t>(i) * kTile;
-          if (g > 0) {
-            ok = mbar_wait(smem_u32(&bars->do_empty), (g - 1) & 1, abort, a.status);
-            if (!ok) break;
-          }
-          {
-            const uint32_t bar = smem_u32(&bars->do_full);
-            mbar_arrive_expect_tx(bar, 4 * kQBlk + kTile * 4);
-            for (int cb = 0; cb < 4; ++cb)
-              tma_load_4d(sDO + cb * kQBlk, &tmDO, bar, 64 * cb, i * kTile, hh, bb, pol_qd);
-            cp_bulk_g2s(s0 + kOffDrow, a.Drow + row0, kTile * 4, bar);
-          }
-          if (g > 0) {
-            ok = mbar_wait(smem_u32(&bars->q_empty), (g - 1) & 1, abort, a.status);
-            if (!ok) break;
-          }
-          {
+          auto load_q = [&]() {
+            if (g > 0 && !mbar_wait(smem_u32(&bars->q_empty), (g - 1) & 1, abort, a.status))
+              return false;
             const uint32_t bar = smem_u32(&bars->q_full);
             mbar_arrive_expect_tx(bar, 4 * kQBlk + kTile * 4);
             for (int cb = 0; cb < 4; ++cb)
               tma_load_4d(sQ + cb * kQBlk, &tmQ, bar, 64 * cb, i * kTile, hh, bb, pol_qd);
             cp_bulk_g2s(s0 + kOffLse, a.lse2 + row0, kTile * 4, bar);
-          }
+            return true;
+          };
+          auto load_do = [&]() {
+            if (g > 0 && !mbar_wait(smem_u32(&bars->do_empty), (g - 1) & 1, abort, a.status))
+              return false;
+            const uint32_t bar = smem_u32(&bars->do_full);
+            mbar_arrive_expect_tx(bar, 4 * kQBlk + kTile * 4);
+            for (int cb = 0; cb < 4; ++cb)
+              tma_load_4d(sDO + cb * kQBlk, &tmDO, bar, 64 * cb, i * kTile, hh, bb, pol_qd);
+            cp_bulk_g2s(s0 + kOffDrow, a.Drow + row0, kTile * 4, bar);
+            return true;
+          };
+          // the copies follow the order in which the MMAs release the buffers
+          ok = CAUSAL ? (load_do() && load_q()) : (load_q() && load_do());
+          if (!ok) break;
         }
       }
       // producer tail: the consumers have released everything issued before
@@ -279,12 +280,22 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             if (!ok) break;
           }
           tc_fence_after();
+          // non-causal: dK first, so Q_i is released for the next block's
+          // copy, which the next block's first MMA (S) waits for; causal
+          // measured marginally faster with dV first
+          if constexpr (!CAUSAL) {
+            issue_g(tmem + kColDK, sQ, 0, sDS, !first);
+            issue_g(tmem + kColDK + 64, sQ, 1, sDS, !first);
+            mma_commit(smem_u32(&bars->q_empty));
+          }
           issue_g(tmem + kColDV, sDO, 0, sP, !first);
           issue_g(tmem + kColDV + 64, sDO, 1, sP, !first);
           mma_commit(smem_u32(&bars->do_empty));
-          issue_g(tmem + kColDK, sQ, 0, sDS, !first);
-          issue_g(tmem + kColDK + 64, sQ, 1, sDS, !first);
-          mma_commit(smem_u32(&bars->q_empty));
+          if constexpr (CAUSAL) {
+            issue_g(tmem + kColDK, sQ, 0, sDS, !first);
+            issue_g(tmem + kColDK + 64, sQ, 1, sDS, !first);
+            mma_commit(smem_u32(&bars->q_empty));
+          }
           for (int h = 0; h < 2 && ok; ++h) {
             const uint32_t c = 2 * g + h;  // dQ^T halves issued so far
             if (c > 0) {  // the read-out has taken the previous half
