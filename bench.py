@@ -61,7 +61,9 @@ VARLEN_WORKLOADS = {"varlen_d128_s16_256to4096": (16, 16, 128, 256, 4096, 7),
 # second; one step = one fa_decode call.
 DECODE_WORKLOADS = {"decode_b32_h32_nq1_nk8192_d128": (32, 32, 1, 8192, 128),
                     "decode_b1_h32_nq1_nk131072_d128": (1, 32, 1, 131072, 128),
-                    "decode_b32_h32_nq4_nk8192_d128": (32, 32, 4, 8192, 128)}
+                    "decode_b32_h32_nq4_nk8192_d128": (32, 32, 4, 8192, 128),
+                    "decode_b32_h32_nq8_nk8192_d128": (32, 32, 8, 8192, 128),
+                    "decode_b32_h32_nq16_nk8192_d128": (32, 32, 16, 8192, 128)}
 DECODE_METRIC = "attention decode: KV-cache GB/s read (bf16, 1 GB300)"
 
 
@@ -81,7 +83,8 @@ def varlen_lengths(name):
 # workload and causal flag; None where no capture of the current kernel exists.
 # Algorithmic bytes for comparison: q, k, v, dO read and dk, dv written once
 # (6 x 64 MiB) plus the fp32 dQ accumulator (128 MiB) = 537 MB at either size.
-NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.191e8}
+NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.191e8,
+                           ("dim_d256_n4096", False): 6.317e8}
 
 
 def fwd_flops(B, H, N, d, causal):

@@ -123,6 +123,13 @@ __global__ void varlen_check_kernel(const int* cu_q, const int* cu_k, int B, int
   if (bad) atomicCAS(status, DEV_OK, DEV_BADARG);
 }
 
+// Checks per-sequence key counts (see launch_klens_check).
+__global__ void klens_check_kernel(const int* lens, int B, int Nk, int* status) {
+  bool bad = false;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) bad |= lens[b] < 0 || lens[b] > Nk;
+  if (bad) atomicCAS(status, DEV_OK, DEV_BADARG);
+}
+
 // Evaluates the forward kernel's FMA-pipe exp2 on n inputs.
 __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -145,6 +152,11 @@ cudaError_t current_device_setup(int* num_sms, int** status) {
   *num_sms = di.num_sms;
   *status = di.status;
   return cudaSuccess;
+}
+
+cudaError_t launch_klens_check(const int* lens, int B, int Nk, int* status, cudaStream_t stream) {
+  klens_check_kernel<<<1, 256, 0, stream>>>(lens, B, Nk, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_varlen_check(const Problem& p, cudaStream_t stream) {
@@ -507,8 +519,22 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
                   : fa::contiguous_strides(H, kv ? Nk : Nq, d);
   }
   p.Nk = Nk;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (Nq >= fa::kDecodeTensorMinQ && static_cast<int64_t>(B) * H >= di.num_sms) {
+    // enough (batch, head) pairs to fill the SMs without splitting the keys:
+    // the tensor-core forward over a dense batch with per-sequence key counts
+    p.var = 1;
+    p.rows_q = p.max_q = Nq;
+    p.rows_k = p.max_k = Nk;
+    p.cu_k = cache_seqlens;
+    p.klens = cache_seqlens != nullptr;
+    if (p.klens && fa::launch_klens_check(cache_seqlens, B, Nk, p.status, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return fa::launch_fwd(p, q, k_cache, v_cache, o, lse, st) == cudaSuccess ? FA_OK
+                                                                            : FA_ERR_CUDA;
+  }
   const cudaError_t e = fa::launch_decode(p, q, k_cache, v_cache, o, lse, cache_seqlens,
-                                          workspace, static_cast<cudaStream_t>(stream));
+                                          workspace, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

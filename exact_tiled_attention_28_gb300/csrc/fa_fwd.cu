@@ -158,7 +158,7 @@ __device__ __forceinline__ int var_tile_steps(int qt, const Seq& s, bool causal)
   return max(n, 1);
 }
 
-template <int D, bool CAUSAL, bool VAR, bool COMPACT = false>
+template <int D, bool CAUSAL, bool VAR, bool COMPACT = false, bool KLENS = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const typename FwdArgsOf<VAR>::type a) {
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         int hh, bb, q0 = 0, k0 = 0, J;
         if constexpr (VAR) {
-          const Seq sq = seq_of(bh, a.g);
+          const Seq sq = seq_of<KLENS>(bh, a.g);
           hh = sq.hh;
           bb = sq.bb;
           q0 = sq.q0;
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         int Jt[2];
         if constexpr (VAR) {
-          const Seq sq = seq_of(bh, a.g);
+          const Seq sq = seq_of<KLENS>(bh, a.g);
           Jt[0] = var_tile_steps(2 * pair, sq, CAUSAL);
           Jt[1] = var_tile_steps(2 * pair + 1, sq, CAUSAL);
           if (Jt[0] == 0 && Jt[1] == 0) {  // skipped by the loader too: no Q round
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int J;
       int key_lim = 0;  // VAR: the last key this row may see, relative to the sequence
       if constexpr (VAR) {
-        const Seq sq = seq_of(bh, a.g);
+        const Seq sq = seq_of<KLENS>(bh, a.g);
         J = var_tile_steps(qt, sq, CAUSAL);
         key_lim = sq.nk - 1;
         if (CAUSAL) key_lim = min(key_lim, qt * kTile + r + sq.nk - sq.nq);
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __nv_bfloat16* orow;
       Seq sq;
       if constexpr (VAR) {  // a row that saw no key has l = 0: O = 0, LSE = -inf
-        sq = seq_of(bh, a.g);
+        sq = seq_of<KLENS>(bh, a.g);
         store = row < sq.nq;
         inv_l = l > 0.f ? 1.f / l : 0.f;
         orow = a.o + sq.bb * a.so.batch + sq.hh * a.so.head +
@@ -603,12 +603,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool CAUSAL, bool VAR = false, bool COMPACT = false>
+template <int D, bool CAUSAL, bool VAR = false, bool COMPACT = false, bool KLENS = false>
 cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const typename FwdArgsOf<VAR>::type& a,
                          cudaStream_t stream, int extra_smem = 0) {
   const int smem = fwd_smem_bytes<D>() + extra_smem;
-  auto kern = fwd_kernel<D, CAUSAL, VAR, COMPACT>;
+  auto kern = fwd_kernel<D, CAUSAL, VAR, COMPACT, KLENS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = min(a.n_items, p.num_sms);
@@ -625,6 +625,9 @@ cudaError_t launch_var_d(const Problem& p, const CUtensorMap& mq, const CUtensor
   if (a.compact)
     return p.causal ? launch_fwd_t<D, true, true, true>(p, mq, mk, mv, a, stream, extra)
                     : launch_fwd_t<D, false, true, true>(p, mq, mk, mv, a, stream, extra);
+  if (p.klens)  // dense batch with per-sequence key counts
+    return p.causal ? launch_fwd_t<D, true, true, false, true>(p, mq, mk, mv, a, stream)
+                    : launch_fwd_t<D, false, true, false, true>(p, mq, mk, mv, a, stream);
   return p.causal ? launch_fwd_t<D, true, true>(p, mq, mk, mv, a, stream)
                   : launch_fwd_t<D, false, true>(p, mq, mk, mv, a, stream);
 }

@@ -38,7 +38,8 @@ struct Problem {
   int var;
   int Nk;
   const int* cu_q;
-  const int* cu_k;
+  const int* cu_k;  // dense batch with klens = 1: B valid key counts (see seq_of)
+  int klens;
   int rows_q, rows_k, max_q, max_k;
 };
 
@@ -94,6 +95,14 @@ size_t bwd_workspace_bytes(int B, int H, int N, int d);
 // of up to Nk keys (cache_seqlens[b] of them when given), split along the
 // keys over CTAs and merged by log-sum-exp.
 constexpr int kDecodeMaxQ = 16;
+// fa_decode runs N_q >= kDecodeTensorMinQ on the tensor-core forward for a
+// dense batch with per-sequence key counts (no key split) once the B * H
+// (batch, head) pairs fill the SMs. The split-key kernel below does its
+// per-row arithmetic on CUDA cores: on GB300 (B = H = 32, 8192-key cache,
+// d = 128) it read the cache at 7.1 / 6.9 / 5.4 / 3.2 / 1.4 TB/s for
+// N_q = 1 / 2 / 4 / 8 / 16, the tensor-core forward at 5.2-5.4 TB/s for each
+// (at N_q = 4 the two are within run-to-run noise).
+constexpr int kDecodeTensorMinQ = 8;
 constexpr int kDecodeMaxSplits = 256;
 
 struct DecodePlan {
@@ -115,6 +124,10 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
 // sequence, then the fp32 dQ accumulator (and, packed, the compacted work
 // schedule, sized by the longest key sequence max_k).
 size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int max_k, int d);
+
+// Records DEV_BADARG in the status word when one of the B key counts is
+// outside 0..Nk.
+cudaError_t launch_klens_check(const int* lens, int B, int Nk, int* status, cudaStream_t stream);
 
 // Records DEV_BADARG in the status word when the packed batch's offsets are
 // not non-decreasing from 0 to rows_q / rows_k or a length exceeds max_q /

@@ -33,7 +33,10 @@ struct Seq {
 
 // Sequence-and-head index sh = b * H + h. Packed offsets are clamped to the
 // buffers, so that malformed offsets give wrong results but every row index
-// stays inside the tensors (a separate check reports them).
+// stays inside the tensors (a separate check reports them). KLENS: a dense
+// batch whose cu_k holds B per-sequence key counts (a key/value cache with
+// valid lengths), clamped to 0..Nk.
+template <bool KLENS = false>
 __device__ __forceinline__ Seq seq_of(int sh, const VarGeom& g) {
   Seq s;
   const int b = sh / g.H;
@@ -56,7 +59,7 @@ __device__ __forceinline__ Seq seq_of(int sh, const VarGeom& g) {
     s.q0 = 0;
     s.k0 = 0;
     s.nq = g.Nq;
-    s.nk = g.Nk;
+    s.nk = KLENS ? min(max(__ldg(g.cu_k + b), 0), g.Nk) : g.Nk;
     s.pst = 0;
   }
   return s;

@@ -202,6 +202,9 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
  * keys of each (batch, head) split over several thread blocks and the parts
  * merged by their log-sum-exp (the identity behind the online softmax,
  * "Flash Attention v2" notes, "Detailed Algorithm Comparison", forward pass).
+ * With Nq >= 8 and at least as many (batch, head) pairs as the GPU has SMs,
+ * it runs the tensor-core forward over the batch instead (no key split; the
+ * workspace is then unused).
  *  q, o: bf16 [B, H, Nq, d]; k_cache, v_cache: bf16 [B, H, Nk, d]; strides: 12
  *  element strides (batch, head, row) for q, k_cache, v_cache, o as in
  *  fa_fwd_strided (a [B, Nk, H, d] cache is a view), or NULL for contiguous

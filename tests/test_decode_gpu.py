@@ -111,3 +111,45 @@ def test_decode_cache_length_out_of_range_is_reported(cuda_lib):
     cs = torch.tensor([300, 299], dtype=torch.int32, device="cuda")
     fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, True, 0.1, cache_seqlens=cs, workspace=ws)
     assert fa.fa_last_device_status() == fa.FA_OK
+
+
+# More (batch, head) pairs than SMs and Nq >= 8: fa_decode runs the
+# tensor-core forward over the dense batch with per-sequence key counts
+# instead of the split-key kernel. B * H = 160 >= 152 SMs.
+
+@pytest.mark.parametrize("Nq", [8, 13, 16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_tensor_core_path(cuda_lib, Nq, causal):
+    rng = np.random.default_rng(560 + Nq)
+    seqlens = [int(x) for x in rng.integers(1, 701, size=8)]
+    seqlens[:3] = [0, Nq - 2, 700]  # no key, fewer keys than queries, the whole cache
+    _decode(cuda_lib, 560 + Nq, 8, 20, Nq, 700, 128, causal, seqlens=seqlens)
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+def test_decode_tensor_core_path_head_dims(cuda_lib, d):
+    _decode(cuda_lib, 570 + d, 4, 40, 16, 300, d, True, seqlens=[300, 129, 5, 256])
+
+
+def test_decode_tensor_core_path_uniform_cache_and_bnhd(cuda_lib):
+    _decode(cuda_lib, 580, 8, 20, 9, 333, 128, True)
+    _decode(cuda_lib, 581, 8, 20, 12, 1000, 64, False, seqlens=[1000, 1, 0, 999, 500, 128, 129, 2],
+            bnhd=True)
+
+
+def test_decode_tensor_core_path_bad_length_is_reported(cuda_lib):
+    import torch
+    fa = cuda_lib
+    B, H, Nq, Nk, d = 8, 20, 8, 200, 64
+    bits = inputs.nqnk_inputs(590, B, H, Nq, Nk, d)
+    dev = {n: inputs.bits_to_torch_bf16(b).cuda() for n, b in bits.items()}
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(fa.fa_decode_workspace_size(B, H, Nq, Nk, d), 16), dtype=torch.uint8,
+                     device="cuda")
+    cs = torch.tensor([200] * 7 + [-1], dtype=torch.int32, device="cuda")
+    fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, True, 0.1, cache_seqlens=cs, workspace=ws)
+    assert fa.fa_last_device_status() == fa.FA_ERR_INVALID_ARG
+    cs = torch.tensor([200] * 8, dtype=torch.int32, device="cuda")
+    fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, True, 0.1, cache_seqlens=cs, workspace=ws)
+    assert fa.fa_last_device_status() == fa.FA_OK
