@@ -207,6 +207,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unit-rates", action="store_true",
+                    help="measure the MUFU exp2 and FP32 FMA rates (the softmax's "
+                         "secondary roofs) and print them as one JSON line")
     return ap.parse_args()
 
 
@@ -808,8 +811,44 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_unit_rates(args):
+    """The secondary roofs next to the tensor pipe: MUFU exp2 and FP32 FMA
+    operations per clock per SM, and the bf16 tensor rate per SM for
+    comparison (the measured burst peak over the SM count and its clock)."""
+    import torch
+
+    import exact_tiled_attention_28_gb300 as fa
+    torch.cuda.set_device(0)
+    fa.load()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(0).uuid)
+    except Exception:
+        pass
+    fa.fa_measure_unit_rates(256)  # warm-up
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    r = fa.fa_measure_unit_rates(8192)
+    clocks = sampler.stop()
+    peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = clocks.get("sm_mhz") or 2070.0
+    tensor_flop_per_clk_sm = peaks["burst"] * 1e12 / sms / (mhz * 1e6)
+    # per score: the forward's two products cost 4 d FLOPs and its softmax one
+    # exp2; the ratio bounds how far the exponentials may fall behind
+    r.update({"unit": "operations per clock per SM", "sms": sms, "clocks": clocks,
+              "tensor_bf16_flop_per_clk_per_sm_burst": tensor_flop_per_clk_sm,
+              "scores_per_clk_per_sm_tensor_d128": tensor_flop_per_clk_sm / (4 * 128),
+              "scores_per_clk_per_sm_tensor_d64": tensor_flop_per_clk_sm / (4 * 64)})
+    print(json.dumps(r), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.unit_rates:
+        run_unit_rates(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     elif args.workload in VARLEN_WORKLOADS:

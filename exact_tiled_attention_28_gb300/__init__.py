@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     fa_fwd,
     fa_fwd_varlen,
     fa_last_device_status,
+    fa_measure_unit_rates,
     fa_selftest_exp2,
     fa_selftest_wait_timeout,
     fa_status_string,

@@ -27,7 +27,7 @@ EXPORTED = ("fa_abi_version", "fa_fwd", "fa_fwd_strided", "fa_bwd_workspace_size
             "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout", "fa_selftest_exp2",
             "fa_status_string", "fa_last_device_status", "fa_fwd_nqnk", "fa_bwd_nqnk",
             "fa_fwd_varlen", "fa_bwd_varlen_workspace_size", "fa_bwd_varlen",
-            "fa_decode_workspace_size", "fa_decode")
+            "fa_decode_workspace_size", "fa_decode", "fa_measure_unit_rates")
 
 # fixed device scratch of fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in include/fa.h)
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -81,6 +81,8 @@ def load():
     lib.fa_selftest_exp2.argtypes = [vp, vp, i, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
+    lib.fa_measure_unit_rates.restype = i
+    lib.fa_measure_unit_rates.argtypes = [vp, i, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [i]
     lib.fa_last_device_status.restype = i
@@ -202,6 +204,23 @@ def fa_bwd_noalloc_raw(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, causal, scal
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_measure_unit_rates(iters: int = 4096) -> dict:
+    """Runs the arithmetic-unit microbenchmark on the current device and
+    returns operations per clock per SM for the MUFU exp2 (ex2.approx), FFMA
+    and the two-lane FFMA2 (counted in FMAs), with the cycle counts. Waits for
+    the device (a measurement, not a step of the attention path)."""
+    import torch
+    cyc = torch.zeros(6, dtype=torch.int64, device="cuda")
+    _check(load().fa_measure_unit_rates(cyc.data_ptr(), int(iters), _stream_handle(None)),
+           "fa_measure_unit_rates")
+    torch.cuda.synchronize()
+    c = [int(x) for x in cyc.cpu()]
+    ops = 2 * 1024 * 8 * int(iters)  # per SM, per kernel
+    return {"ex2_per_clk_per_sm": ops / c[0], "ffma_per_clk_per_sm": ops / c[2],
+            "ffma2_fma_per_clk_per_sm": 2 * ops / c[4], "cycles": [c[0], c[2], c[4]],
+            "iters": int(iters)}
 
 
 def fa_selftest_wait_timeout(limit_ms: int, stream=None) -> None:

@@ -538,6 +538,18 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_measure_unit_rates(unsigned long long* cycles, int iters, void* stream) {
+  if (cycles == nullptr || (reinterpret_cast<uintptr_t>(cycles) & 7u) != 0 || iters < 1 ||
+      iters > (1 << 20))
+    return FA_ERR_INVALID_ARG;
+  fa::DeviceInfo di;
+  if (fa::device_info(&di) != cudaSuccess) return FA_ERR_CUDA;
+  return fa::launch_unit_rates(cycles, iters, di.num_sms, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
 fa_status fa_selftest_wait_timeout(int limit_ms, void* stream) {
   if (limit_ms < 1 || limit_ms > 2000) return FA_ERR_INVALID_ARG;
   fa::DeviceInfo di;

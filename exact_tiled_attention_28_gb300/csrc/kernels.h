@@ -125,6 +125,11 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
 // schedule, sized by the longest key sequence max_k).
 size_t bwd_var_workspace_bytes(bool packed, int B, int H, int rows_q, int max_k, int d);
 
+// The arithmetic-unit microbenchmark (fa_unit_rates.cu): writes the largest
+// block cycle count of the ex2, FFMA and FFMA2 kernels to cycles[0], [2], [4].
+cudaError_t launch_unit_rates(unsigned long long* cycles, int iters, int num_sms,
+                              cudaStream_t stream);
+
 // Records DEV_BADARG in the status word when one of the B key counts is
 // outside 0..Nk.
 cudaError_t launch_klens_check(const int* lens, int B, int Nk, int* status, cudaStream_t stream);

@@ -225,6 +225,20 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
                     size_t workspace_bytes, void* stream);
 
 /*
+ * Microbenchmark of the arithmetic units the softmax runs on (no counterpart
+ * in the method; it measures the secondary roofs next to the tensor pipe):
+ * enqueues three kernels that run independent chains of ex2.approx.ftz.f32
+ * (the MUFU exponential), fma.rn.f32 and the two-lane fma.rn.f32x2 on every SM,
+ * 2 blocks x 1024 threads x 8 chains x iters instructions per SM each.
+ * cycles: DEVICE array of 6 unsigned 64-bit values, 8-byte aligned; after the
+ * stream reaches the call, cycles[0], [2] and [4] hold the largest block's
+ * clock64 cycle count of the ex2, FFMA and FFMA2 kernel (cycles[1], [3], [5]
+ * are scratch). Operations per clock per SM = 16384 x iters / cycles (twice
+ * that for FFMA2, which does two FMAs per instruction). iters in 1..2^20.
+ */
+fa_status fa_measure_unit_rates(unsigned long long* cycles, int iters, void* stream);
+
+/*
  * Self-test of the failure path (no counterpart in the method): enqueues a
  * one-thread kernel that waits on an on-chip barrier nothing ever arrives on,
  * with a limit of limit_ms milliseconds (1..2000) instead of the 2 s the

@@ -223,3 +223,10 @@ def test_d256_dense_forward_and_backward_only(lib):
         fa.FA_ERR_UNSUPPORTED
     assert lib.fa_decode(P, P, P, P, P, None, 1, 1, 1, 100, 256, None, 0, 0.1, None, 0, None) == \
         fa.FA_ERR_UNSUPPORTED
+
+
+def test_unit_rates_rejects_before_launch(lib):
+    assert lib.fa_measure_unit_rates(None, 16, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_measure_unit_rates(P + 4, 16, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_measure_unit_rates(P, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_measure_unit_rates(P, (1 << 20) + 1, None) == fa.FA_ERR_INVALID_ARG
