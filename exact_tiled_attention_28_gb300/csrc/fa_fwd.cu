@@ -498,7 +498,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // p = 2^(s * scale*log2e - m * scale*log2e), two lanes per instruction
         const float2 sl2v = make_float2(sl2, sl2);
-        const float2 negv = make_float2(-m_use * sl2, -m_use * sl2);
+        // Masked scores are already -inf, so they give 2^-inf = 0 without a
+        // select in the loop below (selects there cost 12% of the forward at
+        // d = 128 and 20% at d = 64). A row that has seen no key yet keeps
+        // m = -inf; 0 in its place keeps its arguments -inf instead of NaN.
+        const float m_safe = m_use == NEG_INF ? 0.f : m_use;
+        const float2 negv = make_float2(-m_safe * sl2, -m_safe * sl2);
         uint32_t pk[64];
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
@@ -513,10 +518,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           } else {
             p0 = ex2_approx(x.x);
             p1 = ex2_approx(x.y);
-          }
-          if (masked) {
-            p0 = (2 * c > lim) ? 0.f : p0;
-            p1 = (2 * c + 1 > lim) ? 0.f : p1;
           }
           acc[c & 3] = fadd2(acc[c & 3], make_float2(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
@@ -649,7 +650,7 @@ cudaError_t launch_fwd_var(const Problem& p, const void* q, const void* k, const
   a.n_pairs = ((p.max_q + kTile - 1) / kTile + 1) / 2;
   a.n_items = a.BH * a.n_pairs;
   a.scale = p.scale;
-  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.scale_log2 = fwd_scale_log2(p.scale);
   a.so = p.st[kO];
   a.g = VarGeom{p.cu_q, p.cu_k, p.H, p.N, p.Nk, p.rows_q, p.rows_k, p.max_q, p.max_k};
   a.n_seq = p.B;
@@ -710,7 +711,7 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const voi
   a.n_pairs = (a.n_tiles + 1) / 2;
   a.n_items = BH * a.n_pairs;
   a.scale = p.scale;
-  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.scale_log2 = fwd_scale_log2(p.scale);
   switch (p.d) {
     case 32:
       return p.causal ? launch_fwd_t<32, true>(p, mq, mk, mv, a, stream)
