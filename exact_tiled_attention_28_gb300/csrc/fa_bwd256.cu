@@ -343,23 +343,37 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         int lim = min(kKeys - 1, a.N - 1 - j * kKeys);
         if (CAUSAL && i == i0) lim = min(lim, i * kTile + r - j * kKeys);
         const uint32_t prow = sP + r * 128, drow = sDS + r * 128;
+        // P and dS for 32 key columns; `mask` applies the causal diagonal and
+        // the keys past N. Two copies of the loop, so that blocks with nothing
+        // to mask (all but the diagonal and the last) run no select: selects
+        // in the loop cost 12% of the kernel.
+        const bool masked = lim < kKeys - 1;
+        auto p_ds = [&](int c, const uint32_t (&sv)[32], const uint32_t (&dv)[32], bool mask,
+                        uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int k0 = 32 * c + 2 * t;
+            float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * t]), sl2, -l2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * t + 1]), sl2, -l2));
+            if (mask) {
+              p0 = k0 > lim ? 0.f : p0;
+              p1 = k0 + 1 > lim ? 0.f : p1;
+            }
+            pk[t] = pack_bf16x2(p0, p1);
+            dk[t] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * t]) - dr),
+                                p1 * (__uint_as_float(dv[2 * t + 1]) - dr));
+          }
+        };
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sv[32], dv[32];
           tmem_ld32(t_lane + kColS + 32 * c, sv);
           tmem_ld32(t_lane + kColDP + 32 * c, dv);
           uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const int k0 = 32 * c + 2 * t;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * t]), sl2, -l2));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * t + 1]), sl2, -l2));
-            p0 = k0 > lim ? 0.f : p0;
-            p1 = k0 + 1 > lim ? 0.f : p1;
-            pk[t] = pack_bf16x2(p0, p1);
-            dk[t] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * t]) - dr),
-                                p1 * (__uint_as_float(dv[2 * t + 1]) - dr));
-          }
+          if (masked)
+            p_ds(c, sv, dv, true, pk, dk);
+          else
+            p_ds(c, sv, dv, false, pk, dk);
           // 16-byte chunk m of the row's 128 bytes sits at chunk m ^ (row & 7)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {

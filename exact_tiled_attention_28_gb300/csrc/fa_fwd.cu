@@ -650,7 +650,7 @@ cudaError_t launch_fwd_var(const Problem& p, const void* q, const void* k, const
   a.n_pairs = ((p.max_q + kTile - 1) / kTile + 1) / 2;
   a.n_items = a.BH * a.n_pairs;
   a.scale = p.scale;
-  a.scale_log2 = fwd_scale_log2(p.scale);
+  a.scale_log2 = clamped_scale_log2(p.scale);
   a.so = p.st[kO];
   a.g = VarGeom{p.cu_q, p.cu_k, p.H, p.N, p.Nk, p.rows_q, p.rows_k, p.max_q, p.max_k};
   a.n_seq = p.B;
@@ -711,7 +711,7 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const voi
   a.n_pairs = (a.n_tiles + 1) / 2;
   a.n_items = BH * a.n_pairs;
   a.scale = p.scale;
-  a.scale_log2 = fwd_scale_log2(p.scale);
+  a.scale_log2 = clamped_scale_log2(p.scale);
   switch (p.d) {
     case 32:
       return p.causal ? launch_fwd_t<32, true>(p, mq, mk, mv, a, stream)

@@ -453,7 +453,7 @@ cudaError_t launch_fwd256(const Problem& p, const void* q, const void* k, const 
   a.n_tiles = (p.N + kTile - 1) / kTile;
   a.n_items = a.BH * a.n_tiles;
   a.scale = p.scale;
-  a.scale_log2 = fwd_scale_log2(p.scale);
+  a.scale_log2 = clamped_scale_log2(p.scale);
   a.so = p.st[kO];
   return p.causal ? launch256_t<true>(p, mq, mk, mv, a, stream)
                   : launch256_t<false>(p, mq, mk, mv, a, stream);

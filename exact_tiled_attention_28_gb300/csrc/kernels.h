@@ -54,12 +54,12 @@ inline Strides contiguous_strides(int H, int N, int d) {
 bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
                    const Strides& s, int box_rows = kTile);
 
-// scale * log2(e) for the forward kernels, at least 1e-30. The forward turns
-// masked scores into 2^-inf = 0 through their -inf value alone, which needs
-// a positive factor (-inf * 0 is NaN); at scale = 0 the clamp changes the
-// exponent of an unmasked score by |s| * 1e-30, i.e. nothing, and the log-sum-
-// exp keeps its max term from the true scale.
-inline float fwd_scale_log2(float scale) {
+// scale * log2(e), at least 1e-30, for the kernels that turn masked scores
+// into 2^-inf = 0 through their -inf value alone (the forwards), which needs
+// a positive factor (-inf * 0 is NaN). At scale = 0
+// the clamp changes the exponent of an unmasked score by |s| * 1e-30, i.e.
+// nothing; the log-sum-exp keeps its max term from the true scale.
+inline float clamped_scale_log2(float scale) {
   const float f = scale * 1.4426950408889634f;
   return f > 1e-30f ? f : 1e-30f;
 }
