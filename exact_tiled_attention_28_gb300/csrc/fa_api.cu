@@ -186,7 +186,7 @@ bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int 
 
 extern "C" {
 
-int fa_abi_version(void) { return 1; }
+int fa_abi_version(void) { return 2; }
 
 const char* fa_status_string(int status) {
   switch (status) {

@@ -58,7 +58,9 @@ typedef enum fa_status {
   FA_ERR_WORKSPACE = 5    /* backward workspace null or too small */
 } fa_status;
 
-/* Version of this ABI; bumped on any incompatible change. */
+/* Version of this ABI; bumped on any incompatible change. 2: the packed
+ * backward's workspace size also takes the longest key length
+ * (fa_bwd_varlen_workspace_size). */
 int fa_abi_version(void);
 
 /*
