@@ -153,3 +153,35 @@ def test_decode_tensor_core_path_bad_length_is_reported(cuda_lib):
     cs = torch.tensor([200] * 8, dtype=torch.int32, device="cuda")
     fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, True, 0.1, cache_seqlens=cs, workspace=ws)
     assert fa.fa_last_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("Nq", [1, 16])
+def test_decode_bench_cache_sampled(cuda_lib, Nq):
+    """The bench's decode cache (8192 keys, valid lengths in [4096, 8192],
+    d = 128, H = 32) with B = 8, so that B * H still exceeds the SM count and
+    both paths run in the bench's launch configuration: Nq = 1 the split-key
+    kernel with one split per head, Nq = 16 the tensor-core forward. Every
+    row finite; six sampled heads against the oracle."""
+    import torch
+    fa = cuda_lib
+    B, H, Nk, d, causal = 8, 32, 8192, 128, True
+    scale = gu.default_scale(d)
+    seqlens = [int(n) for n in np.random.default_rng(9).integers(Nk // 2, Nk + 1, size=B)]
+    bits = inputs.nqnk_inputs(595 + Nq, B, H, Nq, Nk, d)
+    dev = {n: inputs.bits_to_torch_bf16(b).cuda() for n, b in bits.items()}
+    o = torch.full_like(dev["q"], float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    cs = torch.tensor(seqlens, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(fa.fa_decode_workspace_size(B, H, Nq, Nk, d), 16), dtype=torch.uint8,
+                     device="cuda")
+    fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, causal, scale, cache_seqlens=cs,
+                 workspace=ws)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    og, lg = gu.to_f64(o), gu.to_f64(lse)
+    assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg))
+    for b, h in gu.sample_heads(B, H, 6, seed=Nq):
+        nk = seqlens[b]
+        x = {n: inputs.bf16_bits_to_f64(bits[n][b, h, :nk] if n != "q" else bits[n][b, h])
+             for n in ("q", "k", "v")}
+        ow, lw = oracle.head_forward(x["q"], x["k"], x["v"], causal, scale)
+        gu.check_o_lse(og[b, h], lg[b, h], ow, lw, f"Nq={Nq} b={b} h={h} nk={nk}")
