@@ -246,3 +246,41 @@ def test_varlen_many_short_sequences(cuda_lib, n_seq, d):
                                max(lens_k), causal, gu.default_scale(d))
         assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
         assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_bench_batch_sampled(cuda_lib, causal):
+    """The bench's packed batch (16 sequences of 276..3885 tokens, H = 16,
+    d = 128): every output finite, and three sampled (sequence, head) blocks
+    against the oracle, forward and backward (sequences are independent)."""
+    import torch
+    fa = cuda_lib
+    lens = [int(n) for n in np.random.default_rng(7).integers(256, 4097, size=16)]
+    H, d = 16, 128
+    scale = gu.default_scale(d)
+    bits, cu_q, cu_k = inputs.packed_inputs(420, lens, lens, H, d)
+    dev = _to_dev(bits)
+    T = int(cu_q[-1])
+    cq = torch.tensor(cu_q, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty((H, T), dtype=torch.float32, device="cuda")
+    fa.fa_fwd_varlen(dev["q"], dev["k"], dev["v"], o, lse, cq, cq, max(lens), max(lens), causal,
+                     scale)
+    ws = torch.empty(fa.fa_bwd_varlen_workspace_size(16, H, T, max(lens), d), dtype=torch.uint8,
+                     device="cuda")
+    dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
+    fa.fa_bwd_varlen(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], dq, dk, dv, cq, cq,
+                     max(lens), max(lens), causal, scale, ws)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    g = {n: gu.to_f64(t) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    for t in g.values():
+        assert np.all(np.isfinite(t))
+    rng = np.random.default_rng(421)
+    for b, h in [(int(rng.integers(16)), int(rng.integers(H))) for _ in range(3)]:
+        r0, r1 = int(cu_q[b]), int(cu_q[b + 1])
+        x = {n: inputs.bf16_bits_to_f64(bits[n][r0:r1, h]) for n in ("q", "k", "v", "do")}
+        ow, lw = oracle.head_forward(x["q"], x["k"], x["v"], causal, scale)
+        gu.check_o_lse(g["o"][r0:r1, h], g["lse"][h, r0:r1], ow, lw, f"b={b} h={h}")
+        want = oracle.head_backward(x["q"], x["k"], x["v"], x["do"], causal, scale)
+        gu.check_grads((g["dq"][r0:r1, h], g["dk"][r0:r1, h], g["dv"][r0:r1, h]), want,
+                       f"b={b} h={h} n={r1 - r0}")
