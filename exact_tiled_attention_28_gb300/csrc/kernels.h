@@ -35,12 +35,12 @@ struct Problem {
   // rows cu_q[b]..cu_q[b+1]-1 of q and cu_k[b]..cu_k[b+1]-1 of k and v,
   // which hold rows_q and rows_k rows per head (batch coordinate 0); max_q
   // and max_k bound the lengths.
-  int var;
-  int Nk;
-  const int* cu_q;
-  const int* cu_k;  // dense batch with klens = 1: B valid key counts (see seq_of)
-  int klens;
-  int rows_q, rows_k, max_q, max_k;
+  int var = 0;
+  int Nk = 0;
+  const int* cu_q = nullptr;
+  const int* cu_k = nullptr;  // dense batch with klens = 1: B valid key counts (see seq_of)
+  int klens = 0;
+  int rows_q = 0, rows_k = 0, max_q = 0, max_k = 0;
 };
 
 // Contiguous [B, H, N, d] strides.
