@@ -25,9 +25,10 @@
 // Shared memory (224 KiB + rows): Q_i and dO_i (128 x 256 bf16 each), K_j and
 // V_j (64 x 256 each), P and dS (128 x 64 each, written by the compute warps
 // in the 128-byte swizzled layout the MMAs read), the lse2 and D rows of
-// block i. There is room for one Q_i / dO_i buffer only. The dK MMAs run
-// first and release Q_i, whose successor the next block's S needs first; dO_i
-// follows after the dV MMAs; both copies overlap the dQ^T MMAs.
+// block i. There is room for one Q_i / dO_i buffer only. Non-causal, the dK
+// MMAs run first and release Q_i, whose successor the next block's S needs
+// first, and dO_i follows after the dV MMAs; causal keeps dV first (measured
+// marginally faster). Both copies overlap the dQ^T MMAs.
 //
 // 384 threads: warp 0 TMA loader, warp 1 MMA issuer, warps 4-7 compute (one
 // thread per query row = TMEM lane), warps 8-11 dQ^T read-out and the dK /
