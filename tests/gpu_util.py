@@ -7,12 +7,18 @@ LSE max-abs <= 1e-3 (LSE is a sum of fp32 terms of size ln N, far more
 accurate than bf16 outputs; 1e-3 leaves room for the fp32 row sum at
 N = 32768).
 
-O is stored in bf16, whose spacing is 2^-5 for values in [4, 8): storing the
-exact value alone can be off by half of that, 0.0156, more than the 1e-2
-bound. The max-abs bound is therefore applied to the error in excess of that
-storage rounding, |o - o_ref| - ulp_bf16(o_ref) / 2, which is the kernel's own
-error; for |o_ref| < 1 the two differ by at most 2^-9. The relative-L2 bound
-is applied to the raw difference.
+O's max-abs bound is asserted on the raw difference |o - o_ref| for every
+element with |o_ref| < 2. From |o_ref| = 2 up, storing O in bf16 alone can be
+off by half a bf16 spacing, 2^-7 = 0.0078 on [2, 4) and 0.0156 on [4, 8),
+and the P.V product takes P rounded to bf16 (relative error up to 2^-9): a
+float simulation of the kernel's arithmetic over the first 64 causal rows of
+1500 seeded heads reached a raw error of 1.008e-2 on [2, 4) (7.4e-3 on
+[1, 2)). There the bound applies to the error in excess of that storage
+rounding, |o - o_ref| - ulp_bf16(o_ref) / 2. The relative-L2 bound is always
+applied to the raw difference. The raw form is the bound the configurations
+carry, all at scale = 1/sqrt(d); tests at other scales (a peaked softmax at 4x
+that scale puts more weight on few bf16-rounded P values) pass raw=False and
+take the beyond-storage form everywhere.
 """
 
 from __future__ import annotations
@@ -97,15 +103,28 @@ def max_abs_beyond_bf16_storage(got, want):
     return float(np.max(np.abs(got - want) - half_ulp_bf16(want)))
 
 
-def check_o_lse(o_got, lse_got, o_want, lse_want, what=""):
+# |O_ref| from which the max-abs bound is taken beyond the bf16 storage rounding
+O_RAW_BELOW = 2.0
+
+
+def o_max_abs(got, want, raw=True):
+    """(raw max-abs over |want| < 2, max-abs beyond bf16 storage over |want| >= 2);
+    raw=False: (0, the beyond-storage form over every element)."""
+    small = np.abs(want) < O_RAW_BELOW if raw else np.zeros(want.shape, bool)
+    return max_abs(got[small], want[small]), max_abs_beyond_bf16_storage(got[~small], want[~small])
+
+
+def check_o_lse(o_got, lse_got, o_want, lse_want, what="", raw=True):
     assert np.all(np.isfinite(o_got)), f"{what}: non-finite O"
     assert np.all(np.isfinite(lse_got)), f"{what}: non-finite LSE"
-    ma, rl = max_abs_beyond_bf16_storage(o_got, o_want), rel_l2(o_got, o_want)
+    raw, beyond = o_max_abs(o_got, o_want, raw)
+    rl = rel_l2(o_got, o_want)
     ml = max_abs(lse_got, lse_want)
-    assert ma <= TOL_O_MAXABS, f"{what}: O max-abs beyond bf16 storage {ma:.3e}"
+    assert raw <= TOL_O_MAXABS, f"{what}: O max-abs {raw:.3e} (|O_ref| < 2)"
+    assert beyond <= TOL_O_MAXABS, f"{what}: O max-abs beyond bf16 storage {beyond:.3e} (|O_ref| >= 2)"
     assert rl <= TOL_O_RELL2, f"{what}: O rel-L2 {rl:.3e}"
     assert ml <= TOL_LSE_MAXABS, f"{what}: LSE max-abs {ml:.3e}"
-    return ma, rl, ml
+    return max(raw, beyond), rl, ml
 
 
 def check_grads(got, want, what=""):
