@@ -5,7 +5,11 @@ Python binding of the C ABI in ``include/fa.h`` (``libfa.so``). See
 """
 
 from .binding import (  # noqa: F401
+    FA_DQ_ATOMIC,
+    FA_DQ_AUTO,
+    FA_DQ_SEPARATE,
     FA_ERR_CUDA,
+    FA_ERR_DEVICE_CHECK,
     FA_ERR_INVALID_ARG,
     FA_ERR_TIMEOUT,
     FA_ERR_UNSUPPORTED,
@@ -25,6 +29,10 @@ from .binding import (  # noqa: F401
     fa_measure_unit_rates,
     fa_selftest_exp2,
     fa_selftest_wait_timeout,
+    fa_set_wait_limit_ns,
+    fa_is_debug_build,
+    fa_selftest_index_check,
+    use_library,
     fa_status_string,
     library_path,
     load,

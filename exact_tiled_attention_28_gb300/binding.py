@@ -20,19 +20,28 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
+FA_ERR_DEVICE_CHECK = 6
 
 # every symbol include/fa.h declares
 EXPORTED = ("fa_abi_version", "fa_fwd", "fa_fwd_strided", "fa_bwd_workspace_size", "fa_bwd",
             "fa_bwd_strided", "fa_bwd_preprocess",
-            "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_selftest_wait_timeout", "fa_selftest_exp2",
+            "fa_bwd_dkdv", "fa_bwd_dq_finalize", "fa_bwd_noalloc", "fa_bwd_with_dq_path", "fa_selftest_wait_timeout",
+            "fa_set_wait_limit_ns", "fa_is_debug_build", "fa_selftest_index_check",
+            "fa_selftest_exp2",
             "fa_status_string", "fa_last_device_status", "fa_fwd_nqnk", "fa_bwd_nqnk",
             "fa_fwd_varlen", "fa_bwd_varlen_workspace_size", "fa_bwd_varlen",
             "fa_decode_workspace_size", "fa_decode", "fa_measure_unit_rates")
 
+# dq_path of fa_bwd_with_dq_path
+FA_DQ_AUTO, FA_DQ_ATOMIC, FA_DQ_SEPARATE = 0, 1, 2
+
 # fixed device scratch of fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in include/fa.h)
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+# default limit of the kernels' bounded waits (FA_WAIT_LIMIT_NS_DEFAULT)
+WAIT_LIMIT_NS_DEFAULT = 2_000_000_000
 
-_lib = None
+_lib = None      # the library every call below goes through
+_loaded = {}     # debug flag -> loaded library
 
 
 class FaError(RuntimeError):
@@ -41,16 +50,34 @@ class FaError(RuntimeError):
         super().__init__(f"{where}: {status_string_safe(status)}")
 
 
-def library_path() -> str:
-    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+def library_path(debug: bool = False) -> str:
+    """libfa.so, or with debug=True the debug build libfa_debug.so (index
+    checks on every store, settable wait limit; include/fa.h)."""
+    name = "libfa_debug.so" if debug else "libfa.so"
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), name)
+
+
+def use_library(debug: bool):
+    """Routes every later call through the release (False) or the debug (True)
+    library; returns the one used before, as a debug flag."""
+    global _lib
+    before = _lib is not None and _lib is _loaded.get(True)
+    _lib = _load_path(bool(debug))
+    return before
 
 
 def load():
     """Loads libfa.so (once) and declares the C signatures. Raises if absent."""
     global _lib
-    if _lib is not None:
-        return _lib
-    path = library_path()
+    if _lib is None:
+        _lib = _load_path(False)
+    return _lib
+
+
+def _load_path(debug: bool):
+    if debug in _loaded:
+        return _loaded[debug]
+    path = library_path(debug)
     if not os.path.exists(path):
         raise FaError(FA_ERR_CUDA, f"{path} is not built; run __graft_entry__.build()")
     lib = ctypes.CDLL(path)
@@ -75,12 +102,20 @@ def load():
     lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.fa_bwd_dq_finalize.restype = i
     lib.fa_bwd_dq_finalize.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_with_dq_path.restype = i
+    lib.fa_bwd_with_dq_path.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_selftest_exp2.restype = i
     lib.fa_selftest_exp2.argtypes = [vp, vp, i, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
+    lib.fa_set_wait_limit_ns.restype = i
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_is_debug_build.restype = i
+    lib.fa_is_debug_build.argtypes = []
+    lib.fa_selftest_index_check.restype = i
+    lib.fa_selftest_index_check.argtypes = [vp]
     lib.fa_measure_unit_rates.restype = i
     lib.fa_measure_unit_rates.argtypes = [vp, i, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -101,7 +136,7 @@ def load():
     lib.fa_decode_workspace_size.argtypes = [i] * 5
     lib.fa_decode.restype = i
     lib.fa_decode.argtypes = [vp] * 6 + [i] * 5 + [ll, i, f, vp, sz, vp]
-    _lib = lib
+    _loaded[debug] = lib
     return lib
 
 
@@ -228,6 +263,21 @@ def fa_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
            "fa_selftest_wait_timeout")
 
 
+def fa_set_wait_limit_ns(limit_ns: int) -> None:
+    """Debug build: the limit of every bounded on-chip wait of the kernels (0 =
+    give up at once when a wait does not complete at its first try)."""
+    _check(load().fa_set_wait_limit_ns(int(limit_ns)), "fa_set_wait_limit_ns")
+
+
+def fa_is_debug_build() -> bool:
+    return bool(load().fa_is_debug_build())
+
+
+def fa_selftest_index_check(stream=None) -> None:
+    """Debug build: a kernel whose one index check fails (no memory access)."""
+    _check(load().fa_selftest_index_check(_stream_handle(stream)), "fa_selftest_index_check")
+
+
 def fa_selftest_exp2(x, y, stream=None) -> None:
     """y <- 2^x with the forward kernel's FMA-pipe exponential (CUDA fp32 tensors)."""
     import torch
@@ -273,10 +323,12 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
 
 
 def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace,
-           stream=None) -> None:
+           stream=None, dq_path=None) -> None:
     """dq, dk, dv <- gradients of sum(o * do); workspace is a CUDA uint8 tensor of at
     least fa_bwd_workspace_size(B, H, Nq, d) bytes. Shapes as for fa_fwd (dk, dv
-    like k, dq and do like q)."""
+    like k, dq and do like q). dq_path (FA_DQ_ATOMIC, FA_DQ_SEPARATE or
+    FA_DQ_AUTO) goes through fa_bwd_with_dq_path; it takes contiguous
+    [B, H, N, d] tensors of equal query and key lengths."""
     import torch
     B, H, N, d = _shape(q)
     Nk = int(k.shape[2]) if k.dim() == 4 else -1
@@ -288,7 +340,13 @@ def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspac
     _check_workspace(workspace)
     ptrs = [p["q"], p["k"], p["v"], p["o"], pl, p["do"], p["dq"], p["dk"], p["dv"]]
     st = _strides([t for t, _ in ts])
-    if Nk != N:
+    if dq_path is not None:
+        if Nk != N or st is not None:
+            raise ValueError("dq_path takes contiguous [B, H, N, d] tensors of one length N")
+        _check(load().fa_bwd_with_dq_path(*ptrs, B, H, N, d, int(bool(causal)), float(scale),
+                                          int(dq_path), workspace.data_ptr(), workspace.numel(),
+                                          _stream_handle(stream)), "fa_bwd_with_dq_path")
+    elif Nk != N:
         _check(load().fa_bwd_nqnk(*ptrs, B, H, N, Nk, d, st, int(bool(causal)), float(scale),
                                   workspace.data_ptr(), workspace.numel(),
                                   _stream_handle(stream)), "fa_bwd_nqnk")

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -15,9 +16,14 @@
 
 namespace fa {
 
-// The status word of every kernel in this library; a bounded wait that runs
-// out records DEV_TIMEOUT here.
-__device__ int g_device_status = 0;
+// The status word of every kernel in this library, with the bounded-wait
+// limit beside it (ptx.cuh, DeviceWord); a bounded wait that runs out records
+// DEV_TIMEOUT in the status member.
+__device__ DeviceWord g_device_word = {DEV_OK, 0, kWaitLimitNs};
+
+// Device address of the no-alloc backward's fixed scratch array
+// (fa_noalloc.cu), looked up with the device current.
+cudaError_t noalloc_scratch_lookup(void** out);
 
 namespace {
 
@@ -25,39 +31,74 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
   bool ready = false;
+  unsigned long long ctx_id = 0;  // the CUDA context the addresses below belong to
   int num_sms = 0;
   int* status = nullptr;
+  void* scratch = nullptr;  // fa_bwd_noalloc's array
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
 
-// Per-device set-up, done once with that device current.
+cudaError_t driver_entry(const char* name, unsigned version, void** fn) {
+  cudaDriverEntryPointQueryResult q;
+  const cudaError_t e = cudaGetDriverEntryPointByVersion(name, fn, version, cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || *fn == nullptr) return cudaErrorSymbolNotFound;
+  return cudaSuccess;
+}
+
+// Unique id of the context current on this thread, 0 if none is current yet.
+// Ids are never reused within a process, so a context made after
+// cudaDeviceReset has a new one.
+unsigned long long current_ctx_id() {
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Per-device set-up, done with that device current: the SM count, the device
+// addresses of the status word and of the no-alloc scratch array, and the
+// driver entry points. The addresses belong to the device's context, so the
+// set-up is redone when the current context is not the one they were taken in
+// (after cudaDeviceReset). Looking up the scratch array here, at the first
+// call of any entry point on a device, is what loads the module that holds
+// it: CUDA loads modules lazily by default, and the array's device memory is
+// reserved at that load.
 cudaError_t device_info(DeviceInfo* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    if ((e = driver_entry("cuTensorMapEncodeTiled", 12000, &fn)) != cudaSuccess) return e;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    if ((e = driver_entry("cuCtxGetCurrent", 4000, &fn)) != cudaSuccess) return e;
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    if ((e = driver_entry("cuCtxGetId", 12000, &fn)) != cudaSuccess) return e;
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  }
   DeviceInfo& di = g_dev[dev];
-  if (!di.ready) {
+  const unsigned long long ctx = current_ctx_id();
+  if (!di.ready || ctx == 0 || ctx != di.ctx_id) {
+    di.ready = false;
     e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_device_status);
+    e = cudaGetSymbolAddress(&p, g_device_word);  // makes the device's context current
     if (e != cudaSuccess) return e;
-    di.status = static_cast<int*>(p);
-    if (!g_encode) {
-      cudaDriverEntryPointQueryResult q;
-      void* fn = nullptr;
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q);
-      if (e != cudaSuccess) return e;
-      if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    di.ready = true;
+    di.status = &static_cast<DeviceWord*>(p)->status;
+    e = noalloc_scratch_lookup(&di.scratch);
+    if (e != cudaSuccess) return e;
+    di.ctx_id = current_ctx_id();
+    di.ready = di.ctx_id != 0;
   }
   *out = di;
   return cudaSuccess;
@@ -130,6 +171,14 @@ __global__ void klens_check_kernel(const int* lens, int B, int Nk, int* status) 
   if (bad) atomicCAS(status, DEV_OK, DEV_BADARG);
 }
 
+// Debug build: one failed index check (on an index computed at run time from
+// the lane number, so that the compiler cannot drop it); no memory is
+// accessed.
+__global__ void index_check_selftest_kernel(int* status) {
+  const int idx = static_cast<int>(threadIdx.x) + 32;  // one past a 32-element range
+  fa_dcheck(idx < 32, status);
+}
+
 // Evaluates the forward kernel's FMA-pipe exp2 on n inputs.
 __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -145,12 +194,13 @@ __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
 }  // namespace
 
 // Device facts for launchers outside this file (the no-alloc entry point).
-cudaError_t current_device_setup(int* num_sms, int** status) {
+cudaError_t current_device_setup(int* num_sms, int** status, void** scratch) {
   DeviceInfo di;
   const cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return e;
   *num_sms = di.num_sms;
   *status = di.status;
+  *scratch = di.scratch;
   return cudaSuccess;
 }
 
@@ -196,6 +246,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side bounded wait expired";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: backward workspace null or too small";
+    case FA_ERR_DEVICE_CHECK: return "FA_ERR_DEVICE_CHECK: a device-side index check failed (debug build)";
     default: return "unknown fa_status";
   }
 }
@@ -247,13 +298,20 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 namespace {
 
+// The dQ path fa_bwd takes for a shape (FA_DQ_AUTO): the atomic one, which
+// measured faster on GB300 in every case timed (see fa_bwd_with_dq_path).
+bool auto_dq_separate(int /*B*/, int /*H*/, int /*N*/, int /*d*/, int /*causal*/) { return false; }
+
 fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                      int causal, float scale, void* workspace, size_t workspace_bytes, int stages,
                      std::initializer_list<const void*> used, void* stream,
-                     const long long* strides = nullptr) {
+                     const long long* strides = nullptr, int dq_path = FA_DQ_AUTO) {
   fa_status s = fa::check_sizes(B, H, N, d, scale, /*allow256=*/true);
   if (s != FA_OK) return s;
+  if (dq_path != FA_DQ_AUTO && dq_path != FA_DQ_ATOMIC && dq_path != FA_DQ_SEPARATE)
+    return FA_ERR_INVALID_ARG;
+  if (dq_path == FA_DQ_SEPARATE && !fa::bwd_dq_separate_supported(d)) return FA_ERR_UNSUPPORTED;
   s = fa::check_ptrs(used);
   if (s != FA_OK) return s;
   if (strides != nullptr) {
@@ -269,6 +327,9 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   for (int t = 0; t < fa::kNumTensors; ++t)
     p.st[t] = strides != nullptr ? fa::Strides{strides[3 * t], strides[3 * t + 1], strides[3 * t + 2]}
                                  : fa::contiguous_strides(H, N, d);
+  p.dq_separate = dq_path == FA_DQ_SEPARATE ||
+                  (dq_path == FA_DQ_AUTO && fa::bwd_dq_separate_supported(d) &&
+                   auto_dq_separate(B, H, N, d, causal));
   const cudaError_t e = fa::launch_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, workspace, stages,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -281,6 +342,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, workspace,
                     workspace_bytes, fa::kStagesAll, {q, k, v, o, lse, dO, dq, dk, dv}, stream);
+}
+
+fa_status fa_bwd_with_dq_path(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, int causal, float scale, int dq_path,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+                    workspace_bytes, fa::kStagesAll, {q, k, v, o, lse, dO, dq, dk, dv}, stream,
+                    nullptr, dq_path);
 }
 
 fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
@@ -520,9 +590,13 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   }
   p.Nk = Nk;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (Nq >= fa::kDecodeTensorMinQ && static_cast<int64_t>(B) * H >= di.num_sms) {
-    // enough (batch, head) pairs to fill the SMs without splitting the keys:
-    // the tensor-core forward over a dense batch with per-sequence key counts
+  const int tc_splits = fa::decode_tc_splits(B, H, Nk, di.num_sms);
+  const bool fill = static_cast<int64_t>(B) * H >= di.num_sms;
+  if (Nq >= fa::kDecodeTensorMinQ && (fill || (tc_splits > 1 && fa::fwd_split_supported(d)))) {
+    // the tensor-core forward over a dense batch with per-sequence key
+    // counts: over whole caches when the (batch, head) pairs fill the SMs,
+    // else with the keys split by the decode plan and the splits merged by
+    // log-sum-exp
     p.var = 1;
     p.rows_q = p.max_q = Nq;
     p.rows_k = p.max_k = Nk;
@@ -530,8 +604,17 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
     p.klens = cache_seqlens != nullptr;
     if (p.klens && fa::launch_klens_check(cache_seqlens, B, Nk, p.status, st) != cudaSuccess)
       return FA_ERR_CUDA;
-    return fa::launch_fwd(p, q, k_cache, v_cache, o, lse, st) == cudaSuccess ? FA_OK
-                                                                            : FA_ERR_CUDA;
+    if (fill)
+      return fa::launch_fwd(p, q, k_cache, v_cache, o, lse, st) == cudaSuccess ? FA_OK
+                                                                              : FA_ERR_CUDA;
+    float* part_o = static_cast<float*>(workspace);
+    float* part_lse = part_o + static_cast<size_t>(B) * H * tc_splits * fa::nq_pad_of(Nq) * d;
+    if (fa::launch_fwd_split(p, q, k_cache, v_cache, part_o, part_lse, tc_splits,
+                             fa::nq_pad_of(Nq), st) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return fa::launch_decode_combine(p, part_o, part_lse, tc_splits, o, lse, st) == cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
   }
   const cudaError_t e = fa::launch_decode(p, q, k_cache, v_cache, o, lse, cache_seqlens,
                                           workspace, st);
@@ -572,14 +655,54 @@ fa_status fa_last_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
   int h = 0;
-  if (cudaMemcpyFromSymbol(&h, fa::g_device_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&h, fa::g_device_word, sizeof(int), offsetof(fa::DeviceWord, status)) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
   if (h != fa::DEV_OK) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(fa::g_device_status, &zero, sizeof(int)) != cudaSuccess)
+    if (cudaMemcpyToSymbol(fa::g_device_word, &zero, sizeof(int),
+                           offsetof(fa::DeviceWord, status)) != cudaSuccess)
       return FA_ERR_CUDA;
-    return h == fa::DEV_BADARG ? FA_ERR_INVALID_ARG : FA_ERR_TIMEOUT;
+    if (h == fa::DEV_BADARG) return FA_ERR_INVALID_ARG;
+    return h == fa::DEV_BADINDEX ? FA_ERR_DEVICE_CHECK : FA_ERR_TIMEOUT;
   }
   return FA_OK;
+}
+
+int fa_is_debug_build(void) {
+#ifdef FA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+fa_status fa_set_wait_limit_ns(unsigned long long limit_ns) {
+#ifndef FA_DEBUG
+  (void)limit_ns;
+  return FA_ERR_UNSUPPORTED;  // the release kernels keep the fixed limit
+#else
+  if (limit_ns > fa::kWaitLimitNs) return FA_ERR_INVALID_ARG;
+  fa::DeviceInfo di;
+  if (fa::device_info(&di) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(fa::g_device_word, &limit_ns, sizeof(limit_ns),
+                         offsetof(fa::DeviceWord, wait_limit_ns)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+#endif
+}
+
+fa_status fa_selftest_index_check(void* stream) {
+#ifndef FA_DEBUG
+  (void)stream;
+  return FA_ERR_UNSUPPORTED;  // the release build has no index checks
+#else
+  fa::DeviceInfo di;
+  if (fa::device_info(&di) != cudaSuccess) return FA_ERR_CUDA;
+  fa::index_check_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di.status);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+#endif
 }
 
 }  // extern "C"

@@ -126,6 +126,7 @@ struct PreArgs {
   Workspace ws;
   Strides so, sdo;  // element strides of o and dO
   int N, H, Npad, BH;
+  int zero_acc;  // zero the fp32 dQ accumulator (the atomic dQ path only)
 };
 
 struct DqArgs {
@@ -134,6 +135,7 @@ struct DqArgs {
   Strides sdq;
   int N, H, Npad, BH;
   float scale;
+  int* status;  // debug build: index checks
 };
 
 struct BwdArgs {
@@ -239,9 +241,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
         dot = fmaf(of.x, gf.x, dot);
         dot = fmaf(of.y, gf.y, dot);
       }
-      float4* z = reinterpret_cast<float4*>(dq_acc + e);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.zero_acc) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + e);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     // reduce over the kLanesPerRow consecutive lanes of this row
 #pragma unroll
@@ -327,6 +331,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const DqArgs a, size_t 
     const size_t row = g / (D / 8);  // accumulator row (b*H + h) * N + i
     const int col = static_cast<int>(g % (D / 8)) * 8;
     const int bh = static_cast<int>(row / a.N), i = static_cast<int>(row % a.N);
+    if (!fa_dcheck(FA_IN_SPAN(a.sdq, a.BH / a.H, a.H, a.N, D, row_offset(a.sdq, bh, a.H, i) + col, 8),
+                   a.status))
+      continue;
     uint4 w;
     w.x = pack_bf16x2(x.x * a.scale, x.y * a.scale);
     w.y = pack_bf16x2(x.z * a.scale, x.w * a.scale);
@@ -395,7 +402,10 @@ __device__ __forceinline__ int var_qblock(const KvWork& w, int u, bool causal) {
 // holds one warp of every warpgroup: 4 x 32 x 128 = 16384). The warpgroups then
 // rebalance with setmaxnreg: compute 128, dQ readout 176, load/MMA 80; per
 // sub-partition 128 + 128 + 176 + 80 = 512 registers per lane, the launch total.
-template <int D, bool CAUSAL, bool VAR>
+// DQ = false (the separate dQ path, fa_bwd_dq.cu): no dQ product and no
+// read-out; dS^T stays in TMEM only and both dK orders read it there, as
+// dV(i), S^T(i+1), dK(i), dP^T(i+1).
+template <int D, bool CAUSAL, bool VAR, bool DQ = true>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -651,7 +661,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t stq = sSt + s0 * Cfg::kStageBytes;
         issue_kq(tmem + kColS, sK, stq);
         mma_commit(smem_u32(&bars->s_full));
-        if (it > 0) {
+        if (DQ && it > 0) {
           ok = mbar_wait(smem_u32(&bars->dq_free), (it - 1) & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
@@ -679,7 +689,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = mbar_wait(smem_u32(&bars->ds_ready), it & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
-          if constexpr (CAUSAL) {  // measured faster causal: dK first, dS^T from TMEM
+          if constexpr (!DQ) {  // no dQ product: dK reads dS^T from TMEM
+            issue_acc(tmem + Cfg::col_dk(), tmem + kColDP, stage, u > 0);  // dK += dS^T Q
+          } else if constexpr (CAUSAL) {  // measured faster causal: dK first, dS^T from TMEM
             issue_acc(tmem + Cfg::col_dk(), tmem + kColDP, stage, u > 0);  // dK += dS^T Q
             issue_dq();                                                    // dQ_i = dS K
             mma_commit(smem_u32(&bars->dq_full));
@@ -693,9 +705,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(smem_u32(&bars->acc_done));
             mma_commit(smem_u32(&bars->kv_empty));
           } else {
-            ok = mbar_wait(smem_u32(&bars->dq_free), it & 1, abort, a.status);
-            if (!ok) break;
-            tc_fence_after();
+            if constexpr (DQ) {
+              ok = mbar_wait(smem_u32(&bars->dq_free), it & 1, abort, a.status);
+              if (!ok) break;
+              tc_fence_after();
+            }
             issue_kq(tmem + kColDP, sV, next + Cfg::kTileBytes);  // dP^T(u+1)
             mma_commit(smem_u32(&bars->dp_full));
           }
@@ -822,17 +836,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float2 v = fmul2(pf, g);
             ds[c] = pack_bf16x2(v.x, v.y);
           }
-          if constexpr (CAUSAL) tmem_st16(tDP + 16 * h, ds);  // the causal dK reads it there
+          // the causal dK (and, without dQ, every dK) reads dS^T from TMEM
+          if constexpr (CAUSAL || !DQ) tmem_st16(tDP + 16 * h, ds);
+          if constexpr (DQ) {
 #pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            const int ch = 4 * h + u4;
-            const uint32_t addr = ds_row + ((ch ^ (r & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(ds[4 * u4]),
-                         "r"(ds[4 * u4 + 1]), "r"(ds[4 * u4 + 2]), "r"(ds[4 * u4 + 3])
-                         : "memory");
+            for (int u4 = 0; u4 < 4; ++u4) {
+              const int ch = 4 * h + u4;
+              const uint32_t addr = ds_row + ((ch ^ (r & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(ds[4 * u4]),
+                           "r"(ds[4 * u4 + 1]), "r"(ds[4 * u4 + 2]), "r"(ds[4 * u4 + 3])
+                           : "memory");
+            }
           }
         }
-        fence_proxy_async_smem();
+        if constexpr (DQ) fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
@@ -851,10 +868,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const Strides& so = wg == 0 ? a.sdv : a.sdk;
         out = (wg == 0 ? a.dv : a.dk) + sq.bb * so.batch + sq.hh * so.head +
               static_cast<int64_t>(sq.k0 + key) * so.row;
+#ifdef FA_DEBUG
+        if (store)
+          store = fa_dcheck(in_span(so, a.g.cu_q != nullptr ? 1 : a.BH / a.g.H, a.g.H, a.g.rows_k,
+                                    D, out - (wg == 0 ? a.dv : a.dk), D) &&
+                                FA_IN_RANGE(sq.k0 + key, a.g.rows_k),
+                            a.status);
+#endif
       } else {
         store = key < a.N;
         out = wg == 0 ? a.dv + row_offset(a.sdv, bh, a.H, key)
                       : a.dk + row_offset(a.sdk, bh, a.H, key);
+#ifdef FA_DEBUG
+        if (store)
+          store = fa_dcheck(in_span(wg == 0 ? a.sdv : a.sdk, a.BH / a.H, a.H, a.N, D,
+                                    out - (wg == 0 ? a.dv : a.dk), D),
+                            a.status);
+#endif
       }
       const float mul = wg == 0 ? 1.f : a.scale;
       const uint32_t col = wg == 0 ? kColDV : Cfg::col_dk();
@@ -881,7 +911,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------- dQ warps: add dQ_i
     setmaxnreg_inc<176>();
-    {
+    if constexpr (DQ) {
       const int wq = warp & 3;
       const uint32_t t_lane = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
       uint32_t it = 0;
@@ -931,7 +961,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // All 128 columns go to registers first and TMEM is released
             // before any atomic is issued, so the next dP^T never waits on them.
             const int dd = wq * 32 + lane;
-            const int rows = min(kTile, nq_rows - i * kTile);
+            int rows = min(kTile, nq_rows - i * kTile);
+            if (!fa_dcheck(rows <= 0 || FA_IN_RANGE(i * kTile + rows - 1, nq_rows), a.status))
+              rows = 0;  // debug build: the rows added lie inside the sequence's accumulator
             float* dst = acc_base + static_cast<size_t>(i) * kTile * D + dd;
             uint32_t v[64], w[64];
             tmem_ld64(t_lane + kColDP, v);
@@ -1016,7 +1048,10 @@ cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const PreArg
       if (e != cudaSuccess) return e;
     } else {
       constexpr int smem = bwd_smem_bytes<D>();
-      auto kern = bwd_dkdv_kernel<D, CAUSAL, false>;
+      auto kern = bwd_dkdv_kernel<D, CAUSAL, false, true>;
+      if constexpr (D == 64 || D == 128) {
+        if (p.dq_separate) kern = bwd_dkdv_kernel<D, CAUSAL, false, false>;
+      }
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       const int grid = min(a.n_items, p.num_sms);
@@ -1024,6 +1059,23 @@ cudaError_t launch_bwd_t(const Problem& p, const CUtensorMap* maps, const PreArg
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
+  }
+  if ((stages & kStageDq) && p.dq_separate) {  // the query-stationary dQ kernel (fa_bwd_dq.cu)
+    BwdDqArgs b;
+    b.lse2 = a.ws.lse2(a.BH, a.Npad);
+    b.Drow = a.ws.Drow(a.BH, a.Npad);
+    b.dq = qa.dq;
+    b.status = a.status;
+    b.N = a.N;
+    b.H = a.H;
+    b.Npad = a.Npad;
+    b.BH = a.BH;
+    b.n_tiles = a.n_tiles;
+    b.n_items = a.BH * a.n_tiles;
+    b.scale = a.scale;
+    b.scale_log2 = a.scale_log2;
+    b.sdq = qa.sdq;
+    return launch_bwd_dq_separate(p, maps, b, stream);
   }
   if (stages & kStageDq) {
     const size_t n8 = static_cast<size_t>(a.BH) * a.N * D / 8;
@@ -1124,6 +1176,7 @@ cudaError_t launch_bwd_var(const Problem& p, const void* q, const void* k, const
   qa.Npad = lpad;
   qa.BH = planes;
   qa.scale = p.scale;
+  qa.status = p.status;
   switch (p.d) {
     case 32:
       return p.causal ? launch_bwd_var_t<32, true>(p, maps, pa, a, qa, stream)
@@ -1169,7 +1222,8 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
   const int BH = p.B * p.H;
   CUtensorMap maps[4];
   const int kv_rows = p.d == 256 ? 64 : kTile;  // the d = 256 kernel takes 64-key blocks
-  if ((stages & kStageDkdv) &&
+  if (p.dq_separate && !bwd_dq_separate_supported(p.d)) return cudaErrorInvalidValue;
+  if ((stages & (p.dq_separate ? (kStageDkdv | kStageDq) : kStageDkdv)) &&
       (!make_tile_map(&maps[0], q, p.B, p.H, p.N, p.d, p.st[kQ]) ||
        !make_tile_map(&maps[1], k, p.B, p.H, p.N, p.d, p.st[kK], kv_rows) ||
        !make_tile_map(&maps[2], v, p.B, p.H, p.N, p.d, p.st[kV], kv_rows) ||
@@ -1188,6 +1242,7 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
   pa.H = p.H;
   pa.Npad = n_tiles * kTile;
   pa.BH = BH;
+  pa.zero_acc = p.dq_separate ? 0 : 1;
   BwdArgs a;
   a.ws = ws;
   a.dk = static_cast<__nv_bfloat16*>(dk);
@@ -1212,6 +1267,7 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
   qa.Npad = n_tiles * kTile;
   qa.BH = BH;
   qa.scale = p.scale;
+  qa.status = p.status;
   switch (p.d) {
     case 32:
       return p.causal ? launch_bwd_t<32, true>(p, maps, pa, a, qa, stages, stream)

@@ -407,7 +407,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const int i0 = first_qblock(j, CAUSAL);
       float* const acc_bh = a.dq_acc + static_cast<size_t>(bh) * a.N * 256;
       for (int i = i0; i < a.n_qb && ok; ++i, ++g) {
-        const int rows = min(kTile, a.N - i * kTile);
+        int rows = min(kTile, a.N - i * kTile);
+        if (!fa_dcheck(rows <= 0 || FA_IN_RANGE(i * kTile + rows - 1, a.N), a.status))
+          rows = 0;  // debug build: the rows added lie inside the head's accumulator
         for (int h = 0; h < 2; ++h) {
           const uint32_t c = 2 * g + h;
           ok = mbar_wait_warp(smem_u32(&bars->dq_full), c & 1, abort, a.status);
@@ -437,7 +439,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (!ok) break;
       tc_fence_after();
       const int hh = bh % a.H, bb = bh / a.H;
-      const int keys = min(kKeys, a.N - j * kKeys);
+      int keys = min(kKeys, a.N - j * kKeys);
+      // debug build: the first and the last key row stored lie inside dk and dv
+      if (keys > 0 &&
+          !fa_dcheck(FA_IN_SPAN(a.sdv, a.BH / a.H, a.H, a.N, 256,
+                                bb * a.sdv.batch + hh * a.sdv.head +
+                                    static_cast<int64_t>(j * kKeys + keys - 1) * a.sdv.row, 256) &&
+                         FA_IN_SPAN(a.sdk, a.BH / a.H, a.H, a.N, 256,
+                                    bb * a.sdk.batch + hh * a.sdk.head +
+                                        static_cast<int64_t>(j * kKeys + keys - 1) * a.sdk.row, 256),
+                     a.status))
+        keys = 0;
       for (int h = 0; h < 2; ++h) {
         uint32_t v[64], w[64];
         tmem_ld64(t_lane + kColDV + 64 * h, v);

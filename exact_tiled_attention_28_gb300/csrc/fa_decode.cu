@@ -82,6 +82,7 @@ struct DecodeArgs {
   int H, Nq, Nk, splits, tiles_per_split, causal;
   float scale_log2;
   Strides sq, so;
+  int B;  // debug build: index checks
 };
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
@@ -348,9 +349,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const float out = L > 0.f ? O / L : 0.f;
     const float lse2 = L > 0.f ? M + lg2_approx(L) : NEG_INF;
     if (direct) {
-      if (r < a.Nq) {
-        a.o[b * a.so.batch + h * a.so.head + static_cast<int64_t>(r) * a.so.row + c] =
-            __float2bfloat16_rn(out);
+      const int64_t off = b * a.so.batch + h * a.so.head + static_cast<int64_t>(r) * a.so.row + c;
+      if (r < a.Nq && fa_dcheck(FA_IN_SPAN(a.so, a.B, a.H, a.Nq, D, off, 1), a.status)) {
+        a.o[off] = __float2bfloat16_rn(out);
         if (c == 0)
           a.lse[static_cast<size_t>(bh) * a.Nq + r] =
               lse2 == NEG_INF ? NEG_INF : lse2 * 0.69314718055994531f;
@@ -384,7 +385,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a,
     for (int s = lane; s < a.splits; s += 32)
       L += ex2_approx(a.part_lse[base + static_cast<size_t>(s) * nq_pad] - M);
   L = warp_sum(L);
-  __nv_bfloat16* orow = a.o + b * a.so.batch + h * a.so.head + static_cast<int64_t>(r) * a.so.row;
+  const int64_t roff = b * a.so.batch + h * a.so.head + static_cast<int64_t>(r) * a.so.row;
+  if (!fa_dcheck(FA_IN_SPAN(a.so, a.B, a.H, a.Nq, D, roff, D), a.status)) return;
+  __nv_bfloat16* orow = a.o + roff;
   for (int c = lane; c < D; c += 32) {
     float O = 0.f;
     if (M != NEG_INF) {
@@ -401,11 +404,6 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a,
         L > 0.f ? (M + lg2_approx(L)) * 0.69314718055994531f : NEG_INF;
 }
 
-int nq_pad_of(int Nq) {
-  int n = 1;
-  while (n < Nq) n *= 2;
-  return n;
-}
 
 template <int D, int NQ>
 cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -437,6 +435,37 @@ cudaError_t launch_decode_d(const DecodeArgs& a, const CUtensorMap& mk, const CU
 
 }  // namespace
 
+int nq_pad_of(int Nq) {
+  int n = 1;
+  while (n < Nq) n *= 2;
+  return n;
+}
+
+cudaError_t launch_decode_combine(const Problem& p, const float* part_o, const float* part_lse,
+                                  int splits, void* o, float* lse, cudaStream_t stream) {
+  DecodeArgs a{};
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.part_o = const_cast<float*>(part_o);
+  a.part_lse = const_cast<float*>(part_lse);
+  a.status = p.status;
+  a.H = p.H;
+  a.B = p.B;
+  a.Nq = p.N;
+  a.splits = splits;
+  a.so = p.st[kO];
+  const int rows = p.B * p.H * p.N;
+  const int blocks = (rows + 7) / 8;  // 8 warps per block
+  const int nq_pad = nq_pad_of(p.N);
+  switch (p.d) {
+    case 32: decode_combine_kernel<32><<<blocks, 256, 0, stream>>>(a, nq_pad, rows); break;
+    case 64: decode_combine_kernel<64><<<blocks, 256, 0, stream>>>(a, nq_pad, rows); break;
+    case 96: decode_combine_kernel<96><<<blocks, 256, 0, stream>>>(a, nq_pad, rows); break;
+    default: decode_combine_kernel<128><<<blocks, 256, 0, stream>>>(a, nq_pad, rows); break;
+  }
+  return cudaGetLastError();
+}
+
 // Splits per (batch, head): as many as fit one wave of one CTA per SM (the
 // stages take most of the shared memory), at least one tile per split. On
 // GB300 this beat plans that fill several whole waves (93K valid keys of a
@@ -452,10 +481,35 @@ DecodePlan decode_plan(int B, int H, int Nk, int num_sms) {
   return DecodePlan{(tiles + tps - 1) / tps, tps};
 }
 
+int decode_tc_splits(int B, int H, int Nk, int num_sms) {
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  const int tiles = (Nk + kTile - 1) / kTile;
+  if (bh >= num_sms) return 1;
+  const int lo = static_cast<int>((num_sms + bh - 1) / bh);
+  const int hi = std::max(std::min(tiles, kDecodeMaxSplits), 1);
+  int best = std::min(lo, hi);
+  double best_fill = 0.0;
+  for (int s = std::min(lo, hi); s <= hi; ++s) {
+    const int64_t items = bh * s;
+    const int64_t rounds = (items + num_sms - 1) / num_sms;
+    const double fill = static_cast<double>(items) / static_cast<double>(rounds * num_sms);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = s;
+    }
+    if (fill >= 0.95) break;
+  }
+  return best;
+}
+
 size_t decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_sms) {
   const DecodePlan pl = decode_plan(B, H, Nk, num_sms);
-  if (pl.splits == 1) return 0;
-  return static_cast<size_t>(B) * H * pl.splits * nq_pad_of(Nq) * (d + 1) * 4;
+  int splits = pl.splits == 1 ? 0 : pl.splits;
+  // Nq >= 8 at d = 64 and 128 runs the tensor-core forward with its own split count
+  if (Nq >= kDecodeTensorMinQ && fwd_split_supported(d) && static_cast<int64_t>(B) * H < num_sms)
+    splits = std::max(splits, decode_tc_splits(B, H, Nk, num_sms));
+  if (splits <= 1) return 0;
+  return static_cast<size_t>(B) * H * splits * nq_pad_of(Nq) * (d + 1) * 4;
 }
 
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v, void* o,
@@ -478,6 +532,7 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
   a.cache_seqlens = cache_seqlens;
   a.status = p.status;
   a.H = p.H;
+  a.B = p.B;
   a.Nq = p.N;
   a.Nk = p.Nk;
   a.splits = pl.splits;

@@ -126,6 +126,39 @@ struct FwdArgsOf<true> {
   using type = FwdVarArgs;
 };
 
+// Decode with the keys split over work items (SPLIT, with VAR: a dense batch
+// of Nq <= 16 query rows per sequence against a key/value cache, with or
+// without per-sequence key counts). Item = (b*h, split s); split s covers an
+// even share of the key tiles the sequence's rows see (split_tiles), and
+// writes its rows' O normalised by its own row sum
+// (fp32) and its log-sum-exp in log2 units into the decode workspace, which
+// the decode combine kernel merges by log-sum-exp (the identity the online
+// softmax rests on: "Flash Attention v2" notes, "Detailed Algorithm
+// Comparison", forward pass). A split with no key tile writes -inf and 0.
+struct FwdSplitArgs : FwdVarArgs {
+  float* part_o;    // [B*H, splits, nq_pad, D]
+  float* part_lse;  // [B*H, splits, nq_pad]
+  int splits, nq_pad;
+};
+
+template <bool VAR, bool SPLIT>
+struct FwdArgsSel {
+  using type = typename FwdArgsOf<VAR>::type;
+};
+template <>
+struct FwdArgsSel<true, true> {
+  using type = FwdSplitArgs;
+};
+
+// SPLIT: the split's first key tile t0 and its number of key tiles, out of
+// the J tiles the sequence's rows see from tile 0, divided evenly over the
+// splits (so that sequences shorter than the cache keep every split busy).
+__device__ __forceinline__ int split_tiles(const FwdSplitArgs& a, int split, int J, int& t0) {
+  const int tps = (J + a.splits - 1) / a.splits;
+  t0 = split * tps;
+  return max(0, min(J - t0, tps));
+}
+
 template <class Args>
 __device__ __forceinline__ void decode_item(int item, const Args& a, bool causal, int& bh,
                                             int& pair) {
@@ -158,10 +191,13 @@ __device__ __forceinline__ int var_tile_steps(int qt, const Seq& s, bool causal)
   return max(n, 1);
 }
 
-template <int D, bool CAUSAL, bool VAR, bool COMPACT = false, bool KLENS = false>
+template <int D, bool CAUSAL, bool VAR, bool COMPACT = false, bool KLENS = false,
+          bool SPLIT = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const typename FwdArgsOf<VAR>::type a) {
+               const __grid_constant__ CUtensorMap tmV,
+               const typename FwdArgsSel<VAR, SPLIT>::type a) {
+  static_assert(!SPLIT || (VAR && !COMPACT), "the key split is decode's");
   using Cfg = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -228,15 +264,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
         const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
         if (item >= n_eff) break;  // only in the last, partial round
-        int bh, pair;
+        int bh, pair, split = 0;
         if constexpr (VAR && COMPACT) {
           int b, h;
           sched_decode(sched, a.n_seq, a.n_pairs, a.g.H, CAUSAL, true, item, b, h, pair);
           bh = b * a.g.H + h;
+        } else if constexpr (SPLIT) {
+          bh = item / a.splits;
+          split = item - bh * a.splits;
+          pair = 0;
         } else {
           decode_item(item, a, CAUSAL, bh, pair);
         }
-        int hh, bb, q0 = 0, k0 = 0, J;
+        int hh, bb, q0 = 0, k0 = 0, J, t0 = 0;
         if constexpr (VAR) {
           const Seq sq = seq_of<KLENS>(bh, a.g);
           hh = sq.hh;
@@ -244,6 +284,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           q0 = sq.q0;
           k0 = sq.k0;
           J = max(var_tile_steps(2 * pair, sq, CAUSAL), var_tile_steps(2 * pair + 1, sq, CAUSAL));
+          if constexpr (SPLIT) J = split_tiles(a, split, J, t0);
           if (J == 0) continue;  // every tile of the pair lies past the sequence
         } else {
           hh = bh % a.H;
@@ -272,7 +313,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
             for (int cb = 0; cb < Cfg::kColBlocks; ++cb)
               tma_load_4d(sKV + (s * Cfg::kColBlocks + cb) * kBlockBytes, w ? &tmV : &tmK, bar,
-                          64 * cb, k0 + j * kTile, hh, bb, pol_kv);
+                          64 * cb, k0 + (t0 + j) * kTile, hh, bb, pol_kv);
             ++kv_it;
           }
         }
@@ -330,11 +371,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd, ++q_round) {
         const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
         if (item >= n_eff) break;  // only in the last, partial round
-        int bh, pair;
+        int bh, pair, split = 0;
         if constexpr (VAR && COMPACT) {
           int b, h;
           sched_decode(sched, a.n_seq, a.n_pairs, a.g.H, CAUSAL, true, item, b, h, pair);
           bh = b * a.g.H + h;
+        } else if constexpr (SPLIT) {
+          bh = item / a.splits;
+          split = item - bh * a.splits;
+          pair = 0;
         } else {
           decode_item(item, a, CAUSAL, bh, pair);
         }
@@ -343,6 +388,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const Seq sq = seq_of<KLENS>(bh, a.g);
           Jt[0] = var_tile_steps(2 * pair, sq, CAUSAL);
           Jt[1] = var_tile_steps(2 * pair + 1, sq, CAUSAL);
+          if constexpr (SPLIT) {
+            int t0;
+            Jt[0] = split_tiles(a, split, Jt[0], t0);
+            Jt[1] = split_tiles(a, split, Jt[1], t0);
+          }
           if (Jt[0] == 0 && Jt[1] == 0) {  // skipped by the loader too: no Q round
             --q_round;
             continue;
@@ -433,22 +483,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
       const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
       if (item >= n_eff) break;  // only in the last, partial round
-      int bh, pair;
+      int bh, pair, split = 0;
       if constexpr (VAR && COMPACT) {
         int b, h;
         sched_decode(sched, a.n_seq, a.n_pairs, a.g.H, CAUSAL, true, item, b, h, pair);
         bh = b * a.g.H + h;
+      } else if constexpr (SPLIT) {
+        bh = item / a.splits;
+        split = item - bh * a.splits;
+        pair = 0;
       } else {
         decode_item(item, a, CAUSAL, bh, pair);
       }
       const int qt = 2 * pair + t;
       int J;
       int key_lim = 0;  // VAR: the last key this row may see, relative to the sequence
+      int t0 = 0;       // SPLIT: the split's first key tile
       if constexpr (VAR) {
         const Seq sq = seq_of<KLENS>(bh, a.g);
         J = var_tile_steps(qt, sq, CAUSAL);
         key_lim = sq.nk - 1;
         if (CAUSAL) key_lim = min(key_lim, qt * kTile + r + sq.nk - sq.nq);
+        if constexpr (SPLIT) {
+          J = split_tiles(a, split, J, t0);
+          const int row = qt * kTile + r;
+          if (J == 0 && row < sq.nq) {  // a split past the keys weighs nothing in the merge
+            const size_t part = (static_cast<size_t>(bh) * a.splits + split) * a.nq_pad + row;
+            float4* po = reinterpret_cast<float4*>(a.part_o + part * D);
+            for (int c = 0; c < D / 4; ++c) po[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            a.part_lse[part] = NEG_INF;
+          }
+        }
       } else {
         J = tile_steps(qt, a, CAUSAL);
       }
@@ -466,7 +531,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // masks: causal diagonal tile, and keys past N in the last tile
         int lim = 127;
         if constexpr (VAR) {  // keys past the row's causal limit or past the sequence
-          lim = min(lim, key_lim - j * kTile);
+          lim = min(lim, key_lim - (t0 + j) * kTile);
         } else {
           if (CAUSAL && j == qt) lim = r;
           if (j == a.n_tiles - 1) lim = min(lim, a.N - 1 - j * kTile);
@@ -562,11 +627,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         inv_l = l > 0.f ? 1.f / l : 0.f;
         orow = a.o + sq.bb * a.so.batch + sq.hh * a.so.head +
                static_cast<int64_t>(sq.q0 + row) * a.so.row;
+#ifdef FA_DEBUG  // the batch coordinates span 1 (packed) or the B sequences (dense)
+        if (store)
+          store = fa_dcheck(in_span(a.so, a.g.cu_q != nullptr ? 1 : a.BH / a.g.H, a.g.H,
+                                    a.g.rows_q, D, orow - a.o, D) &&
+                                FA_IN_RANGE(sq.q0 + row, a.g.rows_q),
+                            a.status);
+#endif
       } else {
         store = row < a.N;
         inv_l = 1.f / l;
         orow = a.o + (bh / a.H) * a.so.batch + (bh % a.H) * a.so.head +
                static_cast<int64_t>(row) * a.so.row;
+#ifdef FA_DEBUG
+        if (store) store = fa_dcheck(in_span(a.so, a.BH / a.H, a.H, a.N, D, orow - a.o, D), a.status);
+#endif
+      }
+      if constexpr (SPLIT) {  // the split's normalised rows and log2 LSE, fp32
+        const size_t part = (static_cast<size_t>(bh) * a.splits + split) * a.nq_pad + row;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          if (store) {
+            float4* po = reinterpret_cast<float4*>(a.part_o + part * D + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              po[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
+                                   __uint_as_float(o[4 * v4 + 2]) * inv_l,
+                                   __uint_as_float(o[4 * v4 + 3]) * inv_l);
+          }
+        }
+        if (store)
+          a.part_lse[part] = l > 0.f ? fmaf(m, a.scale * 1.4426950408889634f, lg2_approx(l)) : NEG_INF;
+        continue;
       }
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -604,12 +698,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool CAUSAL, bool VAR = false, bool COMPACT = false, bool KLENS = false>
+template <int D, bool CAUSAL, bool VAR = false, bool COMPACT = false, bool KLENS = false,
+          bool SPLIT = false>
 cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                         const CUtensorMap& mv, const typename FwdArgsOf<VAR>::type& a,
+                         const CUtensorMap& mv, const typename FwdArgsSel<VAR, SPLIT>::type& a,
                          cudaStream_t stream, int extra_smem = 0) {
   const int smem = fwd_smem_bytes<D>() + extra_smem;
-  auto kern = fwd_kernel<D, CAUSAL, VAR, COMPACT, KLENS>;
+  auto kern = fwd_kernel<D, CAUSAL, VAR, COMPACT, KLENS, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = min(a.n_items, p.num_sms);
@@ -675,6 +770,48 @@ cudaError_t launch_fwd_var(const Problem& p, const void* q, const void* k, const
     default:
       return launch_var_d<128>(p, mq, mk, mv, a, stream, extra);
   }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_split_d(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, const FwdSplitArgs& a, cudaStream_t stream) {
+  return p.klens ? launch_fwd_t<D, CAUSAL, true, false, true, true>(p, mq, mk, mv, a, stream)
+                 : launch_fwd_t<D, CAUSAL, true, false, false, true>(p, mq, mk, mv, a, stream);
+}
+
+bool fwd_split_supported(int d) { return d == 64 || d == 128; }
+
+cudaError_t launch_fwd_split(const Problem& p, const void* q, const void* k, const void* v,
+                             float* part_o, float* part_lse, int splits, int nq_pad,
+                             cudaStream_t stream) {
+  if (!fwd_split_supported(p.d) || p.cu_q != nullptr || p.max_q > kTile) return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv;
+  if (!make_tile_map(&mq, q, p.B, p.H, p.rows_q, p.d, p.st[kQ]) ||
+      !make_tile_map(&mk, k, p.B, p.H, p.rows_k, p.d, p.st[kK]) ||
+      !make_tile_map(&mv, v, p.B, p.H, p.rows_k, p.d, p.st[kV]))
+    return cudaErrorInvalidValue;
+  FwdSplitArgs a;
+  a.o = nullptr;
+  a.lse = nullptr;
+  a.status = p.status;
+  a.BH = p.B * p.H;
+  a.n_pairs = 1;
+  a.n_items = a.BH * splits;
+  a.n_seq = p.B;
+  a.compact = 0;
+  a.scale = p.scale;
+  a.scale_log2 = clamped_scale_log2(p.scale);
+  a.so = p.st[kO];
+  a.g = VarGeom{p.cu_q, p.cu_k, p.H, p.N, p.Nk, p.rows_q, p.rows_k, p.max_q, p.max_k};
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.splits = splits;
+  a.nq_pad = nq_pad;
+  if (p.d == 64)
+    return p.causal ? launch_split_d<64, true>(p, mq, mk, mv, a, stream)
+                    : launch_split_d<64, false>(p, mq, mk, mv, a, stream);
+  return p.causal ? launch_split_d<128, true>(p, mq, mk, mv, a, stream)
+                  : launch_split_d<128, false>(p, mq, mk, mv, a, stream);
 }
 
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,

@@ -385,10 +385,13 @@ __global__ void __launch_bounds__(kThreads256, 1)
       if (!ok) break;
       tc_fence_after();
       const int row = qt * kTile + r;
-      const bool store = row < a.N;
+      bool store = row < a.N;
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow = a.o + (bh / a.H) * a.so.batch + (bh % a.H) * a.so.head +
                             static_cast<int64_t>(row) * a.so.row;
+#ifdef FA_DEBUG
+      if (store) store = fa_dcheck(in_span(a.so, a.BH / a.H, a.H, a.N, kD, orow - a.o, kD), a.status);
+#endif
 #pragma unroll 1
       for (int cc = 0; cc < kD / 32; ++cc) {
         uint32_t o[32];

@@ -9,7 +9,10 @@
 // and outputs and nothing is allocated by anyone at call time.
 //
 // The array is file-scope device memory of FA_NOALLOC_SCRATCH_BYTES (32 MiB).
-// Every GPU that loads this library holds it until the process exits. All
+// Every GPU on which any entry point of this library has been called holds it
+// until the process exits: CUDA loads a library's device code lazily, per
+// device, and the library forces that load (and so the reservation of the
+// array) at its first call on each device, whichever entry point it is. All
 // calls share it and it keeps the last call's contents; the backward's first
 // stage rewrites every part of it that later stages read (it zeroes the dQ
 // accumulator and writes the D and log-sum-exp rows), so nothing has to be
@@ -18,48 +21,38 @@
 
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/fa.h"
 #include "kernels.h"
 
 namespace fa {
 
-// device info of the current device (defined in fa_api.cu)
-cudaError_t current_device_setup(int* num_sms, int** status);
+// device facts of the current device (fa_api.cu): the SM count, the status
+// word and this file's scratch array, all as device addresses
+cudaError_t current_device_setup(int* num_sms, int** status, void** scratch);
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// The device address of the scratch array on the current device. In host
-// code g_noalloc_scratch names a host-side stand-in, not device memory, so the
-// address has to come from cudaGetSymbolAddress, once per device, with that
-// device current. The first call on each device does this.
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    if (p == nullptr) return cudaErrorInvalidSymbol;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// The device address of the scratch array on the current device. In host code
+// g_noalloc_scratch names a host-side stand-in, not device memory, so the
+// address has to come from cudaGetSymbolAddress with the device current. The
+// library's per-device set-up (fa_api.cu) calls this at the first call of any
+// entry point on a device, and again in a new context after cudaDeviceReset.
+cudaError_t noalloc_scratch_lookup(void** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  *out = p;
+  return cudaSuccess;
+}
+
 }  // namespace fa
 
 extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
@@ -79,11 +72,10 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
     if (p == nullptr || !fa::aligned16(p)) return FA_ERR_INVALID_ARG;
   // sizes whose workspace does not fit in the fixed array are refused
   if (need > static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  if (fa::scratch_address(&scratch) != cudaSuccess) return FA_ERR_CUDA;
   int num_sms = 0;
   int* status = nullptr;
-  if (fa::current_device_setup(&num_sms, &status) != cudaSuccess) return FA_ERR_CUDA;
+  void* scratch = nullptr;
+  if (fa::current_device_setup(&num_sms, &status, &scratch) != cudaSuccess) return FA_ERR_CUDA;
   fa::Problem p{B, H, N, d, causal ? 1 : 0, scale, num_sms, status, {}};
   for (int t = 0; t < fa::kNumTensors; ++t) p.st[t] = fa::contiguous_strides(H, N, d);
   const cudaError_t e = fa::launch_bwd(p, q, k, v, o, lse, dO, dq, dk, dv, scratch,

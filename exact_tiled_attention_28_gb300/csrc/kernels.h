@@ -41,7 +41,28 @@ struct Problem {
   const int* cu_k = nullptr;  // dense batch with klens = 1: B valid key counts (see seq_of)
   int klens = 0;
   int rows_q = 0, rows_k = 0, max_q = 0, max_k = 0;
+  // Backward of a dense batch: dQ by the query-stationary kernel (fa_bwd_dq.cu)
+  // instead of atomics in the dK/dV kernel (d = 64 and 128).
+  int dq_separate = 0;
 };
+
+// Debug build (FA_DEBUG): whether elements [off, off + n) of a [B, H, rows, d]
+// tensor with these strides lie at or before its last element (and off >= 0).
+// FA_IN_SPAN is that check in the debug build and true (arguments not
+// evaluated) in the release build; kernels pass it to fa_dcheck (ptx.cuh).
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool in_span(const Strides& st, int B, int H, int rows, int d,
+                                        int64_t off, int n) {
+  const int64_t last = static_cast<int64_t>(B - 1) * st.batch + static_cast<int64_t>(H - 1) * st.head +
+                       static_cast<int64_t>(rows - 1) * st.row + d - 1;
+  return off >= 0 && off + n - 1 <= last;
+}
+#define FA_IN_SPAN(st, B, H, rows, d, off, n) ::fa::in_span(st, B, H, rows, d, off, n)
+#define FA_IN_RANGE(i, n) ((i) >= 0 && (i) < (n))
+#else
+#define FA_IN_SPAN(st, B, H, rows, d, off, n) true
+#define FA_IN_RANGE(i, n) true
+#endif
 
 // Contiguous [B, H, N, d] strides.
 inline Strides contiguous_strides(int H, int N, int d) {
@@ -85,6 +106,23 @@ struct Bwd256Args {
 cudaError_t launch_bwd256_dkdv(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mdo,
                                const Bwd256Args& a, cudaStream_t stream);
+// The separate dQ path (fa_bwd_dq.cu): one CTA per (batch*head, 128-row query
+// block) recomputes S and dP against every key block it sees and accumulates
+// dQ in TMEM; writes bf16 dq = scale * dQ directly. lse2 and D are the
+// pre-pass rows [BH, Npad] of the d <= 128 backward.
+struct BwdDqArgs {
+  const float* lse2;
+  const float* Drow;
+  __nv_bfloat16* dq;
+  int* status;
+  int N, H, Npad, BH, n_tiles, n_items;
+  float scale, scale_log2;
+  Strides sdq;
+};
+bool bwd_dq_separate_supported(int d);
+// maps: q, k, v, dO with 128-row boxes.
+cudaError_t launch_bwd_dq_separate(const Problem& p, const CUtensorMap* maps, const BwdDqArgs& a,
+                                   cudaStream_t stream);
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream);
 
@@ -122,6 +160,25 @@ struct DecodePlan {
 
 DecodePlan decode_plan(int B, int H, int Nk, int num_sms);
 size_t decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_sms);
+
+// Decode on the tensor-core forward with the keys split (d = 64 and 128): a
+// dense batch (p.var, p.cu_q null, p.klens as for the forward) of Nq <= 128
+// query rows per sequence; item (b*h, split s) covers an even share of the
+// key tiles the sequence's rows see and writes its normalised rows and log2
+// LSE to part_o [B*H, splits, nq_pad, d] and part_lse [B*H, splits, nq_pad]
+// (splits past the keys: 0 and -inf). launch_decode_combine merges.
+bool fwd_split_supported(int d);
+// Splits per (batch, head) for it: the fewest from ceil(SMs / (B*H)) up
+// whose B*H*splits work items fill their rounds of one item per SM to 95%
+// (the persistent grid takes several rounds), at most one per key tile.
+int decode_tc_splits(int B, int H, int Nk, int num_sms);
+cudaError_t launch_fwd_split(const Problem& p, const void* q, const void* k, const void* v,
+                             float* part_o, float* part_lse, int splits, int nq_pad,
+                             cudaStream_t stream);
+// O = sum_s 2^(lse_s - lse) O_s over the splits, into o (p.st[kO]) and lse.
+cudaError_t launch_decode_combine(const Problem& p, const float* part_o, const float* part_lse,
+                                  int splits, void* o, float* lse, cudaStream_t stream);
+int nq_pad_of(int Nq);
 
 // p.N = Nq, p.Nk = Nk; p.st holds the strides of q, k, v, o (kQ .. kO).
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v, void* o,

@@ -39,6 +39,9 @@
  *  - A kernel that waits on an on-chip barrier for longer than 2 s gives up,
  *    leaves the GPU usable and records FA_ERR_TIMEOUT in a device status word
  *    shared by all calls of the process; fa_last_device_status() reads it.
+ *  - Per-device set-up (SM count, device addresses of the status word and of
+ *    fa_bwd_noalloc's array) is done at the first call on each device, and
+ *    again when the current CUDA context is a new one (after cudaDeviceReset).
  */
 #ifndef FA_H
 #define FA_H
@@ -55,7 +58,8 @@ typedef enum fa_status {
   FA_ERR_UNSUPPORTED = 2, /* head dimension not supported by the call, or B*H too large */
   FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FA_ERR_TIMEOUT = 4,     /* a device-side bounded wait expired */
-  FA_ERR_WORKSPACE = 5    /* backward workspace null or too small */
+  FA_ERR_WORKSPACE = 5,   /* backward workspace null or too small */
+  FA_ERR_DEVICE_CHECK = 6 /* debug build only: a device-side index check failed */
 } fa_status;
 
 /* Version of this ABI; bumped on any incompatible change. 2: the packed
@@ -111,6 +115,30 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd with the path of dQ chosen by the caller. The pages leave open how
+ * the dQ contributions of the key blocks are summed ("Flash Attention v2"
+ * notes, "Backward Pass Computation"; "FlashAttention-2 paper" digest, "Three
+ * changes": work split over query blocks):
+ *  FA_DQ_ATOMIC: the dK/dV kernel adds each (key block, query block) tile's
+ *    dS K to an fp32 accumulator in the workspace with atomic adds, and a
+ *    last pass converts it to bf16 (5 tile products per tile pair). The
+ *    summation order of the atomics varies, so dq may differ in its last
+ *    bits between runs; dk and dv do not.
+ *  FA_DQ_SEPARATE (d = 64 or 128): the dK/dV kernel skips dQ, and a second,
+ *    query-stationary kernel recomputes S and dP for each (query block, key
+ *    block) tile and sums dQ in tensor memory (7 products per tile pair, no
+ *    atomics): dq is the same bits on every run. Other d: FA_ERR_UNSUPPORTED.
+ *  FA_DQ_AUTO: the path fa_bwd takes, the one measured faster for the shape.
+ * Arguments, workspace and errors otherwise as for fa_bwd; an unknown dq_path
+ * returns FA_ERR_INVALID_ARG.
+ */
+enum { FA_DQ_AUTO = 0, FA_DQ_ATOMIC = 1, FA_DQ_SEPARATE = 2 };
+fa_status fa_bwd_with_dq_path(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, int causal, float scale, int dq_path,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa_bwd for strided tensors (see fa_fwd_strided). strides: 24 element
@@ -204,9 +232,11 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
  * keys of each (batch, head) split over several thread blocks and the parts
  * merged by their log-sum-exp (the identity behind the online softmax,
  * "Flash Attention v2" notes, "Detailed Algorithm Comparison", forward pass).
- * With Nq >= 8 and at least as many (batch, head) pairs as the GPU has SMs,
- * it runs the tensor-core forward over the batch instead (no key split; the
- * workspace is then unused).
+ * With Nq >= 8 it runs the tensor-core forward instead: over whole caches
+ * when the (batch, head) pairs are at least as many as the GPU's SMs (the
+ * workspace is then unused), else, at d = 64 and 128, with each sequence's
+ * visible keys divided evenly over a number of splits that fills the SMs,
+ * each split's rows normalised in fp32 and merged by log-sum-exp.
  *  q, o: bf16 [B, H, Nq, d]; k_cache, v_cache: bf16 [B, H, Nk, d]; strides: 12
  *  element strides (batch, head, row) for q, k_cache, v_cache, o as in
  *  fa_fwd_strided (a [B, Nk, H, d] cache is a view), or NULL for contiguous
@@ -257,13 +287,22 @@ fa_status fa_selftest_wait_timeout(int limit_ms, void* stream);
  * deployment variant of fa_bwd.
  *
  * Same arguments, results and errors as fa_bwd, minus the workspace: the
- * library uses a fixed device array of FA_NOALLOC_SCRATCH_BYTES instead,
- * which every GPU that loads libfa.so holds until the process exits. Sizes
- * whose fa_bwd_workspace_size() exceeds that return FA_ERR_WORKSPACE before
- * anything is enqueued (e.g. B*H*N*(d+2) fp32 values must fit in 32 MiB).
- * The call allocates nothing and calls no allocating routine. The first call
- * on each device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.
+ * library uses a fixed device array of FA_NOALLOC_SCRATCH_BYTES instead. The
+ * call is accepted when fa_bwd_workspace_size(B, H, N, d) is at most
+ * FA_NOALLOC_SCRATCH_BYTES, that is when
+ *   4 * (2 * B*H * roundup(N, 128) + B*H*N*d) <= 33554432 bytes
+ * (e.g. B*H = 15 heads of N = 4096 at d = 128); larger sizes return
+ * FA_ERR_WORKSPACE before anything is enqueued. The call allocates nothing
+ * and calls no allocating routine.
+ * When the array is mapped: CUDA loads the library's device code lazily, per
+ * device, and the array's memory is reserved at that load. The library forces
+ * the load at its first call of ANY entry point on a device (that call also
+ * looks up the array's device address with cudaGetSymbolAddress), and keeps
+ * the array until the process exits. So a caller that hands all remaining
+ * device memory to its own pool, or that captures streams into graphs, makes
+ * one library call on each device before doing so; fa_last_device_status(NULL)
+ * is enough. After cudaDeviceReset the next call looks the address up again in
+ * the new context, so the same rule applies after a reset.
  * All calls share the one array and it keeps the last call's contents; the
  * call itself rewrites every part it reads, so nothing needs clearing. Calls
  * that overlap on the GPU (different streams or host threads) race on the
@@ -273,6 +312,35 @@ fa_status fa_selftest_wait_timeout(int limit_ms, void* stream);
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
                          int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * The debug build. The same sources compiled with FA_DEBUG make
+ * libfa_debug.so, with the same entry points. Its kernels (a) take the limit
+ * of their bounded on-chip waits from a device variable that
+ * fa_set_wait_limit_ns sets, and (b) check the indices of their global-memory
+ * stores (row < rows, column < d, offset inside the tensor its strides span)
+ * before each store: a failed check skips the store and records
+ * FA_ERR_DEVICE_CHECK, which fa_last_device_status returns. The release
+ * library (libfa.so) has neither; there these calls return
+ * FA_ERR_UNSUPPORTED. (No counterpart in the method: failure detection.)
+ *
+ * fa_is_debug_build: 1 in libfa_debug.so, 0 in libfa.so.
+ * fa_set_wait_limit_ns: the wall-clock limit, in ns, of every bounded wait of
+ *   the kernels on the current device (default FA_WAIT_LIMIT_NS_DEFAULT, 2 s;
+ *   at most that, else FA_ERR_INVALID_ARG). 0 makes every wait that does not
+ *   complete at its first try give up at once, so the next attention call
+ *   takes its abort path: its roles stop, let the copies in flight land,
+ *   release tensor memory, and the kernel records FA_ERR_TIMEOUT; its outputs
+ *   are then undefined. Synchronises the device; not for use while other
+ *   work of this library runs.
+ * fa_selftest_index_check: enqueues a kernel whose one index check fails (no
+ *   memory is accessed); the next fa_last_device_status returns
+ *   FA_ERR_DEVICE_CHECK.
+ */
+#define FA_WAIT_LIMIT_NS_DEFAULT 2000000000ull
+int fa_is_debug_build(void);
+fa_status fa_set_wait_limit_ns(unsigned long long limit_ns);
+fa_status fa_selftest_index_check(void* stream);
 
 /*
  * Self-test of the forward softmax's FMA-pipe exponential (no counterpart in
@@ -292,6 +360,7 @@ const char* fa_status_string(int status);
  * FA_ERR_INVALID_ARG if a packed batch's offsets broke the rules of
  * fa_fwd_varlen or a decode cache length was outside 0..Nk (the first such
  * record wins; the call clears it),
+ * FA_ERR_DEVICE_CHECK if a debug-build index check failed,
  * FA_ERR_CUDA if the synchronisation failed, else FA_OK.
  */
 fa_status fa_last_device_status(void* stream);

@@ -46,7 +46,7 @@ def test_abi_version(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         s = fa.fa_status_string(code)
         assert s.startswith("FA_")
     assert "unknown" in fa.fa_status_string(99)
@@ -108,11 +108,47 @@ def test_workspace_size(lib):
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """No fallback: without the shared library every call raises."""
     monkeypatch.setattr(binding, "_lib", None)
-    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "libfa.so"))
+    monkeypatch.setattr(binding, "_loaded", {})
+    monkeypatch.setattr(binding, "library_path",
+                        lambda debug=False: str(tmp_path / "libfa.so"))
     with pytest.raises(fa.FaError):
         binding.load()
     with pytest.raises(fa.FaError):
         fa.fa_bwd_workspace_size(1, 1, 128, 64)
+    with pytest.raises(fa.FaError):
+        binding.use_library(True)
+
+
+def test_debug_build_exports_the_same_symbols(lib):
+    """libfa_debug.so (FA_DEBUG: index checks, settable wait limit) has every
+    declared entry point; only it honours the debug hooks."""
+    dbg = binding._load_path(True)
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"{name} not exported by the debug build"
+    assert dbg.fa_is_debug_build() == 1 and lib.fa_is_debug_build() == 0
+    assert lib.fa_set_wait_limit_ns(0) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_selftest_index_check(None) == fa.FA_ERR_UNSUPPORTED
+    # the debug build checks the limit before any device call
+    assert dbg.fa_set_wait_limit_ns(binding.WAIT_LIMIT_NS_DEFAULT + 1) == fa.FA_ERR_INVALID_ARG
+    before = binding.use_library(True)
+    try:
+        assert fa.fa_is_debug_build()
+    finally:
+        binding.use_library(before)
+    assert not fa.fa_is_debug_build()
+
+
+def test_dq_path_rejects_before_launch(lib):
+    def call(path, d=64):
+        return lib.fa_bwd_with_dq_path(*([P] * 9), 1, 2, 256, d, 0, 0.125, path, P,
+                                       fa.fa_bwd_workspace_size(1, 2, 256, d), None)
+    assert call(3) == fa.FA_ERR_INVALID_ARG
+    assert call(-1) == fa.FA_ERR_INVALID_ARG
+    for d in (32, 96, 256):  # the separate dQ kernel takes d = 64 and 128
+        assert call(fa.FA_DQ_SEPARATE, d) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_bwd_with_dq_path(*([P] * 8), None, 1, 2, 256, 64, 0, 0.125, 2, P,
+                                   fa.fa_bwd_workspace_size(1, 2, 256, 64), None) == \
+        fa.FA_ERR_INVALID_ARG
 
 
 def test_library_has_no_torch_dependency(lib):

@@ -185,3 +185,57 @@ def test_decode_bench_cache_sampled(cuda_lib, Nq):
              for n in ("q", "k", "v")}
         ow, lw = oracle.head_forward(x["q"], x["k"], x["v"], causal, scale)
         gu.check_o_lse(og[b, h], lg[b, h], ow, lw, f"Nq={Nq} b={b} h={h} nk={nk}")
+
+
+# Nq >= 8 with fewer (batch, head) pairs than SMs, at d = 64 and 128:
+# fa_decode runs the tensor-core forward with the keys split by the decode
+# plan (each split writes its normalised rows and log2 LSE), then merges the
+# splits by log-sum-exp. Other head dimensions keep the split-key kernel.
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq", [8, 13, 16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_tensor_core_split_keys(cuda_lib, d, Nq, causal):
+    """Per-sequence lengths: no key, fewer keys than queries, a ragged tile,
+    the whole cache; splits past a short sequence's keys weigh nothing."""
+    _decode(cuda_lib, 600 + d + Nq, 4, 3, Nq, 3000, d, causal, seqlens=[0, Nq - 3, 1025, 3000])
+
+
+def test_decode_tensor_core_split_keys_uniform_and_bnhd(cuda_lib):
+    _decode(cuda_lib, 610, 2, 5, 9, 4000, 128, True)
+    _decode(cuda_lib, 611, 3, 4, 16, 2000, 64, False, seqlens=[2000, 1, 777], bnhd=True)
+
+
+def test_decode_other_head_dims_keep_the_split_kernel(cuda_lib):
+    _decode(cuda_lib, 612, 2, 3, 8, 1500, 96, True, seqlens=[1500, 300])
+    _decode(cuda_lib, 613, 2, 3, 16, 1500, 32, False)
+
+
+@pytest.mark.parametrize("Nq", [8, 16])
+def test_decode_long_cache_few_heads_sampled(cuda_lib, Nq):
+    """The bench's long-cache decode shape (B = 1, H = 32, a 131072-key cache
+    with 93K valid keys, d = 128, causal) on the split tensor-core path: every
+    row finite, four sampled heads against the oracle."""
+    import torch
+    fa = cuda_lib
+    B, H, Nk, d, causal = 1, 32, 131072, 128, True
+    scale = gu.default_scale(d)
+    seqlens = [93162]
+    bits = inputs.nqnk_inputs(620 + Nq, B, H, Nq, Nk, d)
+    dev = {n: inputs.bits_to_torch_bf16(b).cuda() for n, b in bits.items()}
+    o = torch.full_like(dev["q"], float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    cs = torch.tensor(seqlens, dtype=torch.int32, device="cuda")
+    ws = torch.full((fa.fa_decode_workspace_size(B, H, Nq, Nk, d),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    fa.fa_decode(dev["q"], dev["k"], dev["v"], o, lse, causal, scale, cache_seqlens=cs,
+                 workspace=ws)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    og, lg = gu.to_f64(o), gu.to_f64(lse)
+    assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg))
+    for b, h in gu.sample_heads(B, H, 4, seed=Nq):
+        nk = seqlens[b]
+        x = {n: inputs.bf16_bits_to_f64(bits[n][b, h, :nk] if n != "q" else bits[n][b, h])
+             for n in ("q", "k", "v")}
+        ow, lw = oracle.head_forward(x["q"], x["k"], x["v"], causal, scale)
+        gu.check_o_lse(og[b, h], lg[b, h], ow, lw, f"Nq={Nq} b={b} h={h} nk={nk}")
