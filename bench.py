@@ -63,7 +63,9 @@ DECODE_WORKLOADS = {"decode_b32_h32_nq1_nk8192_d128": (32, 32, 1, 8192, 128),
                     "decode_b1_h32_nq1_nk131072_d128": (1, 32, 1, 131072, 128),
                     "decode_b32_h32_nq4_nk8192_d128": (32, 32, 4, 8192, 128),
                     "decode_b32_h32_nq8_nk8192_d128": (32, 32, 8, 8192, 128),
-                    "decode_b32_h32_nq16_nk8192_d128": (32, 32, 16, 8192, 128)}
+                    "decode_b32_h32_nq16_nk8192_d128": (32, 32, 16, 8192, 128),
+                    "decode_b1_h32_nq8_nk131072_d128": (1, 32, 8, 131072, 128),
+                    "decode_b1_h32_nq16_nk131072_d128": (1, 32, 16, 131072, 128)}
 DECODE_METRIC = "attention decode: KV-cache GB/s read (bf16, 1 GB300)"
 
 
@@ -186,9 +188,49 @@ def oracle_sample(B, H, N, d, causal, seed, budget_s, max_heads, lengths=None):
     return flops / spent / 1e12, heads, spent
 
 
-def cpu_cores():
-    n = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
-    return int(n) if n and n.isdigit() else os.cpu_count()
+def blas_threads():
+    """Threads of the BLAS library numpy's products run on, read from the
+    library itself: through threadpoolctl where it is installed, else from the
+    OpenBLAS build loaded into this process (its get_num_threads entry point,
+    under the names the numpy and scipy-openblas builds export). Returns
+    (threads, how) or (None, why)."""
+    import numpy as np  # noqa: F401  (loads the BLAS library)
+    try:
+        import threadpoolctl
+        info = [i for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            return max(int(i["num_threads"]) for i in info), "threadpoolctl"
+    except Exception:
+        pass
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f
+                            if "openblas" in ln.lower() and ".so" in ln and "/" in ln})
+    except OSError:
+        paths = []
+    for path in paths:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                    "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn()), f"{os.path.basename(path)}:{sym}"
+    return None, "no BLAS thread count readable"
+
+
+def cpu_cores_entry():
+    """The cpu_baseline's core count: the BLAS threads numpy used (the
+    products); the oracle's elementwise steps run on one thread."""
+    n, how = blas_threads()
+    if n is None:
+        return {"cores": os.cpu_count(), "cores_source": f"os.cpu_count ({how})"}
+    return {"cores": n, "cores_source": f"BLAS threads, read from {how}; "
+                                        "elementwise numpy steps run on one thread"}
 
 
 # ---------------------------------------------------------------------------
@@ -207,6 +249,13 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-legs", action="store_true",
+                    help="skip the sustained leg and the extra workloads of the default line")
+    ap.add_argument("--dq-path-sweep", action="store_true",
+                    help="time the backward's two dQ paths against each other on the GPT-style "
+                         "and long-sequence shapes (one JSON line per shape and mask)")
+    ap.add_argument("--dq-sweep-shapes", default="",
+                    help="comma-separated subset of the dQ path sweep's shapes")
     ap.add_argument("--unit-rates", action="store_true",
                     help="measure the MUFU exp2 and FP32 FMA rates (the softmax's "
                          "secondary roofs) and print them as one JSON line")
@@ -250,7 +299,7 @@ def run_reference(args):
                 "ms_per_step": spent * 1e3 / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": decode_config_of(args, B, H, Nq, Nk, d, dl),
-                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(),
+                "cpu_baseline": {"value": value, "unit": "GB/s", **cpu_cores_entry(),
                                  "kind": "oracle", "sample": "one (sequence, head) block per step"},
                 "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -278,7 +327,7 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": (config_of(args, B, H, N, d) if lengths is None
                        else varlen_config_of(args, lengths, H, d)),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", **cpu_cores_entry(),
                              "kind": "oracle",
                              "sample": f"one head (first sequence, d={d}) fwd+bwd per step"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -463,7 +512,6 @@ def run_varlen(args):
                                                  causal, scale, args.e2e_steps, compute=compute)
     F = sum(fwd_flops(1, H, n, d, causal) for n in lengths)
     peaks = load_peaks()
-    tag = "of " + peaks["source"]
     value = replicas.aggregate_throughput(3.5 * F, world, ms_step_max)
     bwd_tf = 2.5 * F / (bwd_ms * 1e-3) / 1e12
     fwd_tf = F / (fwd_ms * 1e-3) / 1e12
@@ -473,18 +521,13 @@ def run_varlen(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: Q, K, V, dO i.i.d. N(0,1) rounded to bf16, seeded; seeded lengths",
         "config": varlen_config_of(args, lengths, H, d),
-        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_burst_peak": fwd_tf / peaks["burst"],
-                "frac_of_sustained_peak": fwd_tf / peaks["sustained"]},
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_burst_peak": fwd_tf / peaks["burst"]},
         "bwd": {"ms": bwd_ms, "tflops": bwd_tf},
-        "roofline": {"kernel": "fa_bwd_varlen (all stages)", "bound": "tensor",
-                     "achieved": bwd_tf, "peak": peaks["sustained"], "unit": "TFLOP/s",
-                     "frac": bwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}",
-                     "traffic": None,
-                     "algorithmic": f"2.5 x sum_b 4*H*n_b^2*d{' / 2' if causal else ''} = "
-                                    f"{2.5 * F:.4g} FLOP per launch"},
-        "roofline_fwd": {"kernel": "fwd_kernel (packed batch)", "bound": "tensor",
-                         "achieved": fwd_tf, "peak": peaks["sustained"], "unit": "TFLOP/s",
-                         "frac": fwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}"},
+        "roofline": tensor_roofline("fa_bwd_varlen (all stages)", bwd_tf, peaks,
+                                    f"2.5 x sum_b 4*H*n_b^2*d{' / 2' if causal else ''} = "
+                                    f"{2.5 * F:.4g} FLOP per launch"),
+        "roofline_fwd": tensor_roofline("fwd_kernel (packed batch)", fwd_tf, peaks,
+                                        f"{F:.4g} FLOP per launch"),
         "e2e": {"value": 3.5 * F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "two copy-in streams, compute, two copy-out streams; double-buffered",
@@ -497,7 +540,7 @@ def run_varlen(args):
         torch.distributed.barrier()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, heads, spent = oracle_sample(S, H, mx, d, causal, seed, args.cpu_budget_s, 64, lengths)
-        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(),
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", **cpu_cores_entry(),
                                 "kind": "oracle",
                                 "sample": f"{heads} whole (sequence, head) blocks fwd+bwd, "
                                           f"{spent:.1f} s"}
@@ -623,13 +666,24 @@ def run_decode(args):
     peaks = load_peaks()
     gbs = kv_bytes / (ms_step_max * 1e-3) / 1e9 * world
     achieved = algo_bytes / (ms_step * 1e-3) / 1e9
+    # the path fa_decode takes (include/fa.h): Nq >= 8 runs the tensor-core
+    # forward, over whole caches when the (batch, head) pairs fill the SMs,
+    # else with the keys split (d = 64, 128); otherwise the split-key kernel
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    split = B * H < sms and Nk > 128  # more than one key split per (batch, head)
+    if Nq >= 8 and B * H >= sms:
+        kernel, launches = "fwd_kernel (tensor cores, whole caches)", 2
+    elif Nq >= 8 and d in (64, 128) and split:
+        kernel, launches = "fwd_kernel (tensor cores, keys split) + decode_combine_kernel", 3
+    else:
+        kernel, launches = "decode_split_kernel + decode_combine_kernel", 1 + split
     line = {
         "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: q, K, V i.i.d. N(0,1) rounded to bf16, seeded; seeded cache lengths",
         "config": decode_config_of(args, B, H, Nq, Nk, d, lengths),
-        "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel", "bound": "hbm",
+        "roofline": {"kernel": kernel, "bound": "hbm",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "peak_kind": f"copy bandwidth of {peaks['source']}", "traffic": None,
@@ -640,7 +694,7 @@ def run_decode(args):
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": q.numel() * 2,
                 "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
                 "note": "the cache stays on the device; each step copies q in and o, lse out"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
     if world > 1:
@@ -648,13 +702,161 @@ def run_decode(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v_, heads, spent = decode_oracle_sample(B, H, Nq, Nk, d, causal, lengths, seed,
                                                 args.cpu_budget_s, 512)
-        line["cpu_baseline"] = {"value": v_, "unit": "GB/s", "cores": cpu_cores(),
+        line["cpu_baseline"] = {"value": v_, "unit": "GB/s", **cpu_cores_entry(),
                                 "kind": "oracle",
                                 "sample": f"{heads} whole (sequence, head) blocks, {spent:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# Extra points of the default line, each timed like the headline (fwd and the
+# backward's stages with CUDA events): the causal run of the headline
+# workload, the GPT-style d = 64 point at N = 4096 (both masks), the
+# long-sequence causal config and the small d = 64 config.
+SUB_LINES = (("gpt_d128_n4096", True), ("gpt_d64_n4096", False), ("gpt_d64_n4096", True),
+             ("long_b1_h16_n32768_d128", True), ("b4_h8_n1024_d64", False),
+             ("b4_h8_n1024_d64", True))
+
+# Seconds of back-to-back headline steps for the sustained-peak leg: the
+# driver's default run times about 30 ms, where the burst peak applies; the
+# sustained peak is measured on a seconds-long loop, so it is compared only
+# with a loop of that length.
+SUSTAINED_LEG_S = 2.5
+
+
+class Problem:
+    """Device buffers of one dense [B, H, N, d] workload (inputs seeded)."""
+
+    def __init__(self, torch, fa, inputs, dev, seed, B, H, N, d, layout="bhnd", pin=False):
+        self.B, self.H, self.N, self.d = B, H, N, d
+        bits = inputs.attention_inputs(seed, B, H, N, d)
+        host = {n: inputs.bits_to_torch_bf16(b) for n, b in bits.items()}
+        if layout == "bnhd":
+            # [B, N, H, d] storage, passed as [B, H, N, d] views (strided entry points)
+            host = {n: t.transpose(1, 2).contiguous() for n, t in host.items()}
+            if pin:
+                host = {n: t.pin_memory() for n, t in host.items()}
+            host = {n: t.transpose(1, 2) for n, t in host.items()}
+            self.x = {n: t.transpose(1, 2).to(dev).transpose(1, 2) for n, t in host.items()}
+            new = lambda: torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev).transpose(1, 2)
+        else:
+            if pin:
+                host = {n: t.pin_memory() for n, t in host.items()}
+            self.x = {n: t.to(dev) for n, t in host.items()}
+            new = lambda: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        self.host = host
+        self.o = new()
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = new(), new(), new()
+        self.ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        self.layout = layout
+
+    def step(self, fa, stream, causal, scale, ev=None):
+        """fa_fwd + fa_bwd; with ev (6 events): the forward, the backward and
+        its three stages (pre-pass, dK/dV, dQ convert) are bracketed."""
+        x = self.x
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(x["q"], x["k"], x["v"], self.o, self.lse, causal, scale)
+        if ev is not None:
+            ev[1].record(stream)
+        if self.layout == "bhnd":
+            fa.fa_bwd_stages(x["q"], x["k"], x["v"], self.o, self.lse, x["do"], self.dq, self.dk,
+                             self.dv, causal, scale, self.ws,
+                             events=None if ev is None else ev[2:6])
+        else:  # the staged entry points take contiguous tensors: time fa_bwd as a whole
+            if ev is not None:
+                ev[2].record(stream)
+                ev[3].record(stream)
+            fa.fa_bwd(x["q"], x["k"], x["v"], self.o, self.lse, x["do"], self.dq, self.dk,
+                      self.dv, causal, scale, self.ws)
+            if ev is not None:
+                ev[4].record(stream)
+                ev[5].record(stream)
+
+
+def event_means(evs):
+    """Mean ms of fwd, pre-pass, dK/dV, dQ convert and the whole backward."""
+    m = lambda a, b: statistics.mean(e[a].elapsed_time(e[b]) for e in evs)
+    return {"fwd_ms": m(0, 1), "pre_ms": m(2, 3), "dkdv_ms": m(3, 4), "dq_ms": m(4, 5),
+            "bwd_ms": m(2, 5)}
+
+
+def kernel_names(d, layout="bhnd"):
+    if layout != "bhnd":
+        return "fa_bwd (all stages)", "fwd_kernel"
+    return ("bwd256_dkdv_kernel" if d == 256 else "bwd_dkdv_kernel",
+            "fwd256_kernel" if d == 256 else "fwd_kernel")
+
+
+def tensor_roofline(kernel, tflops, peaks, flop, traffic=None):
+    """A tensor-bound roofline entry against the burst bf16 peak (the timed
+    regions here last milliseconds to tens of milliseconds)."""
+    return {"kernel": kernel, "bound": "tensor", "achieved": tflops, "peak": peaks["burst"],
+            "unit": "TFLOP/s", "frac": tflops / peaks["burst"],
+            "peak_kind": f"burst bf16 of {peaks['source']}", "traffic": traffic,
+            "algorithmic": flop}
+
+
+def sub_line(fa, torch, inputs, dev, stream, seed, name, causal, steps, warmup, peaks):
+    """Times one extra workload like the headline; returns its summary."""
+    B, H, N, d = WORKLOADS[name]
+    scale = 1.0 / math.sqrt(d)
+    pb = Problem(torch, fa, inputs, dev, seed, B, H, N, d)
+    for _ in range(max(warmup, 3)):
+        pb.step(fa, stream, causal, scale)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for k in range(steps):
+        pb.step(fa, stream, causal, scale, evs[k])
+    torch.cuda.synchronize()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError(f"device status reports an error in sub-line {name}")
+    t = event_means(evs)
+    F = fwd_flops(B, H, N, d, causal)
+    fwd_tf = F / (t["fwd_ms"] * 1e-3) / 1e12
+    dkdv_tf = 2.5 * F / (t["dkdv_ms"] * 1e-3) / 1e12
+    fb_tf = 3.5 * F / ((t["fwd_ms"] + t["bwd_ms"]) * 1e-3) / 1e12
+    kd, kf = kernel_names(d)
+    del pb
+    torch.cuda.empty_cache()
+    return {"workload": f"{name}: B={B} H={H} N={N} d={d} "
+                        f"{'causal' if causal else 'non-causal'} fwd+bwd",
+            "steps": steps, **{k: v for k, v in t.items()},
+            "fwd_tflops": fwd_tf, "fwd_frac_of_burst_peak": fwd_tf / peaks["burst"],
+            "fwd_bwd_tflops": fb_tf, "fwd_bwd_frac_of_burst_peak": fb_tf / peaks["burst"],
+            "roofline": tensor_roofline(kd, dkdv_tf, peaks, f"2.5 x 4*B*H*N^2*d"
+                                        f"{' / 2' if causal else ''} = {2.5 * F:.4g} FLOP per launch"),
+            "roofline_fwd": tensor_roofline(kf, fwd_tf, peaks, f"{F:.4g} FLOP per launch")}
+
+
+def sustained_leg(fa, torch, pb, stream, causal, scale, seconds, uuid, peaks):
+    """Back-to-back headline steps for at least `seconds`, with the clocks
+    sampled: the throughput a long run settles at, against the sustained peak."""
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    n, wall0 = 0, time.perf_counter()
+    while time.perf_counter() - wall0 < seconds:
+        for _ in range(50):
+            pb.step(fa, stream, causal, scale)
+        n += 50
+        torch.cuda.synchronize()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1)
+    F = fwd_flops(pb.B, pb.H, pb.N, pb.d, causal)
+    tf = 3.5 * F * n / (ms * 1e-3) / 1e12
+    return {"leg": "sustained: back-to-back fwd+bwd steps of the headline workload",
+            "seconds": ms * 1e-3, "steps": n, "fwd_bwd_tflops": tf,
+            "frac_of_sustained_peak": tf / peaks["sustained"],
+            "peak_kind": f"sustained bf16 of {peaks['source']}", "clocks": clocks}
 
 
 def run_ours(args):
@@ -676,44 +878,11 @@ def run_ours(args):
     causal = bool(args.causal)
     scale = 1.0 / math.sqrt(d)
     seed = replicas.replica_seed(1000, rank)
-
-    bits = inputs.attention_inputs(seed, B, H, N, d)
-    host = {n: inputs.bits_to_torch_bf16(b).pin_memory() for n, b in bits.items()}
-    if args.layout == "bnhd":
-        # [B, N, H, d] storage, passed as [B, H, N, d] views (strided entry points)
-        host = {n: t.transpose(1, 2).contiguous().pin_memory().transpose(1, 2)
-                for n, t in host.items()}
-        x = {n: t.transpose(1, 2).to(dev).transpose(1, 2) for n, t in host.items()}
-        new = lambda: torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev).transpose(1, 2)
-    else:
-        x = {n: t.to(dev) for n, t in host.items()}
-        new = lambda: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
-    o = new()
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = new(), new(), new()
-    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    pb = Problem(torch, fa, inputs, dev, seed, B, H, N, d, layout=args.layout, pin=True)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, causal, scale)
-        if ev is not None:
-            ev[1].record(stream)
-        if args.layout == "bhnd":
-            fa.fa_bwd_stages(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, causal, scale,
-                             ws, events=None if ev is None else ev[2:6])
-        else:  # the staged entry points take contiguous tensors: time fa_bwd as a whole
-            if ev is not None:
-                ev[2].record(stream)
-                ev[3].record(stream)
-            fa.fa_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, causal, scale, ws)
-            if ev is not None:
-                ev[4].record(stream)
-                ev[5].record(stream)
-
     for _ in range(max(args.warmup, 3)):
-        step()
+        pb.step(fa, stream, causal, scale)
     if fa.fa_last_device_status() != fa.FA_OK:
         raise RuntimeError("device status reports a timeout during warm-up")
 
@@ -732,7 +901,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_start.record(stream)
     for k in range(args.steps):
-        step(evs[k])
+        pb.step(fa, stream, causal, scale, evs[k])
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -741,11 +910,7 @@ def run_ours(args):
     if fa.fa_last_device_status() != fa.FA_OK:
         raise RuntimeError("device status reports a timeout in the timed region")
     ms_total = t_start.elapsed_time(t_end)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    pre_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    dkdv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
-    dq_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
-    bwd_ms = statistics.mean(e[2].elapsed_time(e[5]) for e in evs)
+    t = event_means(evs)
     ms_step = ms_total / args.steps
 
     ms_step_max = replicas.max_over_ranks(ms_step, dev)
@@ -754,16 +919,18 @@ def run_ours(args):
     # pinned host memory and all of its outputs back. Copies in, compute and
     # copies out run on three streams with double-buffered device tensors, so
     # step k+1's inputs arrive while step k computes and step k-1's outputs leave.
-    e2e_ms, h2d, d2h, h2d_gbs, d2h_gbs = run_e2e(fa, torch, host, x, o, lse, dq, dk, dv, ws,
-                                                 causal, scale, args.e2e_steps)
+    e2e_ms, h2d, d2h, h2d_gbs, d2h_gbs = run_e2e(fa, torch, pb.host, pb.x, pb.o, pb.lse, pb.dq,
+                                                 pb.dk, pb.dv, pb.ws, causal, scale,
+                                                 args.e2e_steps)
 
     F = fwd_flops(B, H, N, d, causal)
     peaks = load_peaks()
-    tag = "of " + peaks["source"]
     value = replicas.aggregate_throughput(3.5 * F, world, ms_step_max)
-    dkdv_tf = 2.5 * F / (dkdv_ms * 1e-3) / 1e12
-    fwd_tf = F / (fwd_ms * 1e-3) / 1e12
+    dkdv_tf = 2.5 * F / (t["dkdv_ms"] * 1e-3) / 1e12
+    fwd_tf = F / (t["fwd_ms"] * 1e-3) / 1e12
+    fb_tf = 3.5 * F / ((t["fwd_ms"] + t["bwd_ms"]) * 1e-3) / 1e12
     traffic = NCU_TRAFFIC_BYTES.get((args.workload, causal)) if args.layout == "bhnd" else None
+    kd, kf = kernel_names(d, args.layout)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -771,25 +938,15 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: Q, K, V, dO i.i.d. N(0,1) rounded to bf16, seeded",
         "config": config_of(args, B, H, N, d),
-        "fwd": {"ms": fwd_ms, "tflops": fwd_tf,
-                "frac_of_burst_peak": fwd_tf / peaks["burst"],
-                "frac_of_sustained_peak": fwd_tf / peaks["sustained"]},
-        "fwd_bwd": {"tflops": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
-                    "frac_of_burst_peak": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peaks["burst"],
-                    "frac_of_sustained_peak": 3.5 * F / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peaks["sustained"]},
-        "bwd": {"ms": bwd_ms, "pre_ms": pre_ms, "dkdv_ms": dkdv_ms, "dq_ms": dq_ms,
-                "tflops": 2.5 * F / (bwd_ms * 1e-3) / 1e12},
-        "roofline": {"kernel": (("bwd256_dkdv_kernel" if d == 256 else "bwd_dkdv_kernel")
-                                if args.layout == "bhnd" else "fa_bwd (all stages)"),
-                     "bound": "tensor", "achieved": dkdv_tf,
-                     "peak": peaks["sustained"], "unit": "TFLOP/s",
-                     "frac": dkdv_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}",
-                     "traffic": traffic,
-                     "algorithmic": f"2.5 x 4*B*H*N^2*d{' / 2' if causal else ''} = {2.5 * F:.4g} FLOP per launch"},
-        "roofline_fwd": {"kernel": "fwd256_kernel" if d == 256 else "fwd_kernel",
-                         "bound": "tensor", "achieved": fwd_tf,
-                         "peak": peaks["sustained"], "unit": "TFLOP/s",
-                         "frac": fwd_tf / peaks["sustained"], "peak_kind": f"sustained bf16 {tag}"},
+        "fwd": {"ms": t["fwd_ms"], "tflops": fwd_tf,
+                "frac_of_burst_peak": fwd_tf / peaks["burst"]},
+        "fwd_bwd": {"tflops": fb_tf, "frac_of_burst_peak": fb_tf / peaks["burst"]},
+        "bwd": {"ms": t["bwd_ms"], "pre_ms": t["pre_ms"], "dkdv_ms": t["dkdv_ms"],
+                "dq_ms": t["dq_ms"], "tflops": 2.5 * F / (t["bwd_ms"] * 1e-3) / 1e12},
+        "roofline": tensor_roofline(kd, dkdv_tf, peaks,
+                                    f"2.5 x 4*B*H*N^2*d{' / 2' if causal else ''} = "
+                                    f"{2.5 * F:.4g} FLOP per launch", traffic),
+        "roofline_fwd": tensor_roofline(kf, fwd_tf, peaks, f"{F:.4g} FLOP per launch"),
         "e2e": {"value": 3.5 * F / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "two copy-in streams, compute, two copy-out streams; double-buffered",
@@ -797,11 +954,20 @@ def run_ours(args):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    if not args.no_extra_legs and args.layout == "bhnd":
+        line["sustained"] = sustained_leg(fa, torch, pb, stream, causal, scale,
+                                          SUSTAINED_LEG_S, uuid, peaks)
+        if args.workload == DEFAULT_WORKLOAD and not causal:
+            del pb
+            torch.cuda.empty_cache()
+            line["sub_lines"] = [sub_line(fa, torch, inputs, dev, stream, seed, name, c,
+                                          min(args.steps, 20), args.warmup, peaks)
+                                 for name, c in SUB_LINES]
     if world > 1:
         torch.distributed.barrier()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, heads, spent = oracle_sample(B, H, N, d, causal, seed, args.cpu_budget_s, 64)
-        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(),
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", **cpu_cores_entry(),
                                 "kind": "oracle",
                                 "sample": f"{heads} whole heads (N={N}, d={d}) fwd+bwd, "
                                           f"{spent:.1f} s"}
@@ -809,6 +975,69 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# The two dQ paths of the backward timed against each other (the atomic
+# accumulation inside the dK/dV kernel, and the dK/dV kernel without dQ plus
+# the query-stationary dQ kernel): name -> (B, H, N, d).
+DQ_SWEEP = {"gpt_d128_n4096": (4, 16, 4096, 128), "gpt_d128_n8192": (2, 16, 8192, 128),
+            "long_b1_h16_n32768_d128": (1, 16, 32768, 128), "gpt_d64_n4096": (4, 32, 4096, 64),
+            "gpt_d64_n8192": (2, 32, 8192, 64), "b1_h32_n32768_d64": (1, 32, 32768, 64)}
+
+
+def run_dq_path_sweep(args):
+    """One JSON line per (shape, mask): fa_bwd_with_dq_path timed with CUDA
+    events on each dQ path (warm-up, then --steps calls each, alternating)."""
+    import torch
+
+    import exact_tiled_attention_28_gb300 as fa
+    from exact_tiled_attention_28_gb300 import inputs
+    torch.cuda.set_device(0)
+    fa.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    shapes = args.dq_sweep_shapes.split(",") if args.dq_sweep_shapes else list(DQ_SWEEP)
+    for name in shapes:
+        B, H, N, d = DQ_SWEEP[name]
+        scale = 1.0 / math.sqrt(d)
+        pb = Problem(torch, fa, inputs, dev, 1000, B, H, N, d)
+        x = pb.x
+        for causal in (False, True):
+            fa.fa_fwd(x["q"], x["k"], x["v"], pb.o, pb.lse, causal, scale)
+
+            def bwd(path):
+                fa.fa_bwd(x["q"], x["k"], x["v"], pb.o, pb.lse, x["do"], pb.dq, pb.dk, pb.dv,
+                          causal, scale, pb.ws, dq_path=path)
+
+            paths = (fa.FA_DQ_ATOMIC, fa.FA_DQ_SEPARATE)
+            for _ in range(max(args.warmup, 3)):
+                for p in paths:
+                    bwd(p)
+            ms = {p: [] for p in paths}
+            for _ in range(args.steps):
+                for p in paths:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    bwd(p)
+                    e1.record(stream)
+                    ms[p].append((e0, e1))
+            torch.cuda.synchronize()
+            if fa.fa_last_device_status() != fa.FA_OK:
+                raise RuntimeError(f"device status reports an error in {name}")
+            F = 2.5 * fwd_flops(B, H, N, d, causal)
+            out = {}
+            for p, label in ((fa.FA_DQ_ATOMIC, "atomic"), (fa.FA_DQ_SEPARATE, "separate")):
+                t = statistics.median(a.elapsed_time(b) for a, b in ms[p])
+                out[label] = {"bwd_ms": t, "bwd_tflops": F / (t * 1e-3) / 1e12,
+                              "frac_of_burst_peak": F / (t * 1e-3) / 1e12 / peaks["burst"]}
+            print(json.dumps({"dq_path_sweep": f"{name}: B={B} H={H} N={N} d={d} "
+                                               f"{'causal' if causal else 'non-causal'}",
+                              "steps": args.steps, **out,
+                              "separate_over_atomic": out["separate"]["bwd_ms"] /
+                                                      out["atomic"]["bwd_ms"]}), flush=True)
+        del pb
+        torch.cuda.empty_cache()
 
 
 def run_unit_rates(args):
@@ -848,6 +1077,9 @@ def main():
     args = parse_args()
     if args.unit_rates:
         run_unit_rates(args)
+        return
+    if args.dq_path_sweep:
+        run_dq_path_sweep(args)
         return
     if args.impl == "reference":
         run_reference(args)
