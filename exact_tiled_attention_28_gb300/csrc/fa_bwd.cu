@@ -40,7 +40,9 @@
 // that its read-out from the dP^T columns overlaps the dK product (dP^T(i+1)
 // waits for that read-out). Causal: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1)
 // with dK reading dS^T from TMEM (the compute warps also store it there);
-// each order measured faster for its case on GB300 (by about 2.5%).
+// each order measured faster for its case on GB300 (by about 2.5%). At
+// d = 64 non-causal: dV(i), dK(i) from TMEM, dQ(i), S^T(i+1), dP^T(i+1)
+// (3% faster there; 13% slower at d = 128).
 
 #include <algorithm>
 
@@ -678,6 +680,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_acc(tmem + kColDV, tmem + kColS, stage + Cfg::kTileBytes, u > 0);  // dV += P^T dO
+          if constexpr (DQ && D == 64 && !CAUSAL) {
+            // d = 64, non-causal: dV(u), dK(u) with dS^T from TMEM, dQ(u),
+            // S^T(u+1), dP^T(u+1), so that S^T(u+1) runs while the dQ read-out
+            // empties the dP^T columns. Measured on GB300 at B = 4, H = 32,
+            // N = 4096: 2.05 against 2.12 ms for the order below; at d = 128
+            // it was 13% slower (8% causal), and causal d = 64 equal.
+            ok = mbar_wait(smem_u32(&bars->ds_ready), it & 1, abort, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_acc(tmem + Cfg::col_dk(), tmem + kColDP, stage, u > 0);  // dK += dS^T Q
+            issue_dq();                                                    // dQ_i = dS K
+            mma_commit(smem_u32(&bars->dq_full));
+            mma_commit(smem_u32(&bars->st_empty[s]));
+            if (!has_next) {
+              mma_commit(smem_u32(&bars->acc_done));
+              mma_commit(smem_u32(&bars->kv_empty));
+            } else {
+              ok = mbar_wait(smem_u32(&bars->st_full[sn]), ((st_it + 1) / Cfg::kStages) & 1, abort,
+                             a.status);
+              if (!ok) break;
+              tc_fence_after();
+              issue_kq(tmem + kColS, sK, next);  // S^T(u+1)
+              mma_commit(smem_u32(&bars->s_full));
+              ok = mbar_wait(smem_u32(&bars->dq_free), it & 1, abort, a.status);
+              if (!ok) break;
+              tc_fence_after();
+              issue_kq(tmem + kColDP, sV, next + Cfg::kTileBytes);  // dP^T(u+1)
+              mma_commit(smem_u32(&bars->dp_full));
+            }
+            continue;
+          }
           if (has_next) {
             ok = mbar_wait(smem_u32(&bars->st_full[sn]), ((st_it + 1) / Cfg::kStages) & 1, abort,
                            a.status);
@@ -836,8 +869,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float2 v = fmul2(pf, g);
             ds[c] = pack_bf16x2(v.x, v.y);
           }
-          // the causal dK (and, without dQ, every dK) reads dS^T from TMEM
-          if constexpr (CAUSAL || !DQ) tmem_st16(tDP + 16 * h, ds);
+          // the causal dK (and without dQ, or at d = 64 non-causal, every dK)
+          // reads dS^T from TMEM
+          if constexpr (CAUSAL || !DQ || D == 64) tmem_st16(tDP + 16 * h, ds);
           if constexpr (DQ) {
 #pragma unroll
             for (int u4 = 0; u4 < 4; ++u4) {
