@@ -74,10 +74,27 @@ struct FwdCfg {
   // TMEM column of S_t and of O_t
   __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+  // d <= 64 can keep Q_t in TMEM too (d / 2 columns of bf16 pairs, after O0
+  // and O1), so that S_t = Q_t K^T reads only K from shared memory. The
+  // tensor core's time is its shared-memory operand reads plus its math
+  // (ncu: tensor pipe active + TC shared-memory wavefronts ~ 95-100% of the
+  // elapsed time in every kernel here), so an A operand from TMEM shortens
+  // each S product. At d = 96 and 128 the four S and O buffers fill TMEM.
+  // Measured on GB300 against Q read from shared memory: non-causal 2.6%
+  // faster at d = 64, N = 4096 (4.0% at N = 16384) and 1.9% at d = 32; the
+  // causal and packed-batch instantiations ran 1.6% and 4% slower (the copy
+  // adds registers where they were at the limit), so only the non-causal,
+  // non-packed ones take it (fwd_kernel's kQT).
+  static constexpr bool kQTmemFits = D <= 64;
+  __device__ static constexpr uint32_t col_q(int t) {
+    return 256u + 2u * static_cast<uint32_t>(D) + static_cast<uint32_t>(D / 2) * t;
+  }
 };
+static_assert(FwdCfg<64>::col_q(1) + 32 <= 512 && FwdCfg<32>::col_q(1) + 16 <= 512,
+              "Q in TMEM past the allocation");
 
 struct FwdBarriers {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[2], q_empty[2], q_tmem[2];
   uint64_t kv_full[8], kv_empty[8];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
@@ -199,6 +216,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                const typename FwdArgsSel<VAR, SPLIT>::type a) {
   static_assert(!SPLIT || (VAR && !COMPACT), "the key split is decode's");
   using Cfg = FwdCfg<D>;
+  constexpr bool kQT = Cfg::kQTmemFits && !CAUSAL && !COMPACT;  // Q_t in TMEM (FwdCfg)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -212,7 +230,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bars->q_full[t]), 1);
-      mbar_init(smem_u32(&bars->q_empty[t]), 1);
+      // kQT: the softmax warps release Q's buffer once they have copied it
+      mbar_init(smem_u32(&bars->q_empty[t]), kQT ? 4 : 1);
+      mbar_init(smem_u32(&bars->q_tmem[t]), 4);
       mbar_init(smem_u32(&bars->s_full[t]), 1);
       mbar_init(smem_u32(&bars->p_full[t]), 4);  // one elected lane per softmax warp
       mbar_init(smem_u32(&bars->o_done[t]), 1);
@@ -341,6 +361,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, false, true);
       uint32_t kv_it = 0, q_round = 0;
       uint32_t step[2] = {0u, 0u};
+      uint32_t qt_round[2] = {0u, 0u};  // kQT: Q copies into TMEM waited for, per tile
       bool ok = true;
 
       // S_t = Q_t K^T over d in steps of 16
@@ -354,7 +375,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          mma_ss(dst, desc_at(da, off), desc_at(db, off), idesc_s, kk > 0);
+          if constexpr (kQT)  // Q_t from TMEM: 8 columns per 16 head dims
+            mma_ts(dst, tmem + Cfg::col_q(t) + 8 * kk, desc_at(db, off), idesc_s, kk > 0);
+          else
+            mma_ss(dst, desc_at(da, off), desc_at(db, off), idesc_s, kk > 0);
         }
       };
       // O_t (+)= P_t V over the 128 keys in steps of 16
@@ -404,8 +428,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int J = max(Jt[0], Jt[1]);
         const uint32_t base = kv_it;
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (ok) ok = mbar_wait(smem_u32(&bars->q_full[t]), q_round & 1, abort, a.status);
+        for (int t = 0; t < 2; ++t) {
+          if constexpr (kQT) {  // the softmax warps copied Q_t into TMEM
+            if (ok && Jt[t] > 0) {
+              ok = mbar_wait(smem_u32(&bars->q_tmem[t]), qt_round[t] & 1, abort, a.status);
+              ++qt_round[t];
+            }
+          } else {
+            if (ok) ok = mbar_wait(smem_u32(&bars->q_full[t]), q_round & 1, abort, a.status);
+          }
+        }
         if (!ok) break;
         tc_fence_after();
         // K_0
@@ -420,7 +452,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               issue_s(t, s);
               mma_commit(smem_u32(&bars->s_full[t]));
             }
-            if (Jt[t] <= 1) mma_commit(smem_u32(&bars->q_empty[t]));
+            if (!kQT && Jt[t] <= 1) mma_commit(smem_u32(&bars->q_empty[t]));
           }
           mma_commit(smem_u32(&bars->kv_empty[s]));
         }
@@ -449,7 +481,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               }
               issue_s(t, sk);
               mma_commit(smem_u32(&bars->s_full[t]));
-              if (j + 2 == Jt[t]) mma_commit(smem_u32(&bars->q_empty[t]));
+              if (!kQT && j + 2 == Jt[t]) mma_commit(smem_u32(&bars->q_empty[t]));
             }
           }
           if (!ok) break;
@@ -479,6 +511,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float sl2 = a.scale_log2;
     const float NEG_INF = __int_as_float(0xff800000);
     uint32_t step = 0;
+    uint32_t q_rounds = 0;  // kQT: Q loads of this tile consumed
     bool ok = true;
     for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < a.n_items && ok; ++rnd) {
       const int item = sched_item(rnd, blockIdx.x, gridDim.x, CAUSAL);
@@ -499,12 +532,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int J;
       int key_lim = 0;  // VAR: the last key this row may see, relative to the sequence
       int t0 = 0;       // SPLIT: the split's first key tile
+      int Jpair = 0;    // kQT: steps of the pair (Q is loaded when > 0)
       if constexpr (VAR) {
         const Seq sq = seq_of<KLENS>(bh, a.g);
         J = var_tile_steps(qt, sq, CAUSAL);
+        if constexpr (kQT) Jpair = max(J, var_tile_steps(2 * pair + 1 - t, sq, CAUSAL));
         key_lim = sq.nk - 1;
         if (CAUSAL) key_lim = min(key_lim, qt * kTile + r + sq.nk - sq.nq);
         if constexpr (SPLIT) {
+          int t1;
+          Jpair = split_tiles(a, split, Jpair, t1);  // the longer tile bounds both
           J = split_tiles(a, split, J, t0);
           const int row = qt * kTile + r;
           if (J == 0 && row < sq.nq) {  // a split past the keys weighs nothing in the merge
@@ -516,6 +553,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       } else {
         J = tile_steps(qt, a, CAUSAL);
+        if constexpr (kQT) Jpair = max(J, tile_steps(2 * pair + 1 - t, a, CAUSAL));
+      }
+      if constexpr (kQT) {
+        // Q_t was loaded for this item when either tile of the pair has steps;
+        // copy row r into TMEM (bf16 pairs, as P is stored), release Q's
+        // buffer, and tell the MMA warp when this tile will use it. The S
+        // products of the previous item read the old copy: every one of them
+        // completed before this warpgroup's waits on s_full returned.
+        if (Jpair > 0) {
+          ok = mbar_wait_warp(smem_u32(&bars->q_full[t]), q_rounds & 1, abort, a.status);
+          if (!ok) break;
+          ++q_rounds;
+          if (J > 0) {
+            const uint32_t qrow = sQ + t * Cfg::kColBlocks * kBlockBytes + r * 128;
+#pragma unroll
+            for (int half = 0; half < D / 32; ++half) {  // 16 columns at a time
+              uint32_t qw[16];
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const int ch = 4 * half + c4;
+                uint4 v;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(qrow + ((ch ^ (r & 7)) << 4)));
+                qw[4 * c4] = v.x;
+                qw[4 * c4 + 1] = v.y;
+                qw[4 * c4 + 2] = v.z;
+                qw[4 * c4 + 3] = v.w;
+              }
+              tmem_st16(t_lane + Cfg::col_q(t) + 16 * half, qw);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bars->q_empty[t]));
+            if (J > 0) mbar_arrive(smem_u32(&bars->q_tmem[t]));
+          }
+        }
       }
       if (J == 0) continue;
       float m = NEG_INF, l = 0.f;
