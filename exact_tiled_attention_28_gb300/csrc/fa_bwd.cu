@@ -77,12 +77,20 @@ struct BwdCfg {
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffDS = 2 * kTileBytes;             // dS^T, 128 x 128 bf16
   static constexpr int kOffStages = 2 * kTileBytes + kTile * kTile * 2;
-  static constexpr int kOffBars = kOffStages + kStages * kStageBytes;
+  // d = 64: a second copy of K_j, the second 64-row half of the dQ_i^T
+  // product's A operand, so that all 128 TMEM lanes of dQ_i^T hold real
+  // values (rows 64-127 repeat rows 0-63) and all four dQ warps share the
+  // read-out and its atomics, half of the query columns each. With rows
+  // 64-127 unused, two warps issued every atomic: on GB300 those took about
+  // 3900 of the 4750 cycles of a query block.
+  static constexpr bool kDupK = D == 64;
+  static constexpr int kOffK2 = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffBars = kOffK2 + (kDupK ? kTileBytes : 0);
   // d >= 64: dQ_i^T = K^T dS^T with M = 128, read out with coalesced atomics.
-  // The MMA's rows past d are never stored: at d = 96 they read the K tile's
-  // zero-filled columns, at d = 64 the V tile that follows K in shared memory
-  // (finite values, results discarded). Measured on GB300 at d = 64 this
-  // still beats dQ_i = dS K with one scattered row per thread by 22%.
+  // At d = 96 the MMA's rows past d read the K tile's zero-filled columns and
+  // are never stored; at d = 64 they read the copy of K (kDupK). Measured on
+  // GB300 at d = 64, with rows 64-127 unused, this beat dQ_i = dS K with one
+  // scattered row per thread by 22%.
   // d = 32: dQ_i = dS K with one row per thread.
   static constexpr bool kDqTransposed = D >= 64;
   static constexpr uint32_t col_dk() { return kColDV + D; }
@@ -424,6 +432,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase + Cfg::kOffK, sV = sbase + Cfg::kOffV, sDS = sbase + Cfg::kOffDS;
   const uint32_t sSt = sbase + Cfg::kOffStages;
+  const uint32_t sK2 = sbase + Cfg::kOffK2;
   BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(smem + Cfg::kOffBars);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5;
@@ -515,11 +524,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         {
           const uint32_t bar = smem_u32(&bars->kv_full);
-          mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
+          constexpr bool kDup = DQ && Cfg::kDupK;
+          mbar_arrive_expect_tx(bar, (kDup ? 3 : 2) * Cfg::kTileBytes);
           for (int cb = 0; cb < Cfg::kColBlocks; ++cb) {
             tma_load_4d(sK + cb * kBlk, &tmK, bar, 64 * cb, k0 + j * kTile, hh, bb, pol_kv);
             tma_load_4d(sV + cb * kBlk, &tmV, bar, 64 * cb, k0 + j * kTile, hh, bb, pol_kv);
           }
+          if constexpr (kDup) tma_load_4d(sK2, &tmK, bar, 0, k0 + j * kTile, hh, bb, pol_kv);
           ++kv_round;
         }
         for (int u = 0; u < n_it && ok; ++u) {
@@ -615,7 +626,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       auto issue_dq = [&]() {
         const SmemDesc d_ds = make_desc_sw128(opaque_u32(sDS), kBlk, 1024);
-        const SmemDesc d_kmn = make_desc_sw128(opaque_u32(sK), kBlk, 1024);
+        const SmemDesc d_kmn =
+            make_desc_sw128(opaque_u32(sK), Cfg::kDupK ? sK2 - sK : kBlk, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t ds_desc = desc_at(d_ds, kk * 2048);
@@ -680,37 +692,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_acc(tmem + kColDV, tmem + kColS, stage + Cfg::kTileBytes, u > 0);  // dV += P^T dO
-          if constexpr (DQ && D == 64 && !CAUSAL) {
-            // d = 64, non-causal: dV(u), dK(u) with dS^T from TMEM, dQ(u),
-            // S^T(u+1), dP^T(u+1), so that S^T(u+1) runs while the dQ read-out
-            // empties the dP^T columns. Measured on GB300 at B = 4, H = 32,
-            // N = 4096: 2.05 against 2.12 ms for the order below; at d = 128
-            // it was 13% slower (8% causal), and causal d = 64 equal.
-            ok = mbar_wait(smem_u32(&bars->ds_ready), it & 1, abort, a.status);
-            if (!ok) break;
-            tc_fence_after();
-            issue_acc(tmem + Cfg::col_dk(), tmem + kColDP, stage, u > 0);  // dK += dS^T Q
-            issue_dq();                                                    // dQ_i = dS K
-            mma_commit(smem_u32(&bars->dq_full));
-            mma_commit(smem_u32(&bars->st_empty[s]));
-            if (!has_next) {
-              mma_commit(smem_u32(&bars->acc_done));
-              mma_commit(smem_u32(&bars->kv_empty));
-            } else {
-              ok = mbar_wait(smem_u32(&bars->st_full[sn]), ((st_it + 1) / Cfg::kStages) & 1, abort,
-                             a.status);
-              if (!ok) break;
-              tc_fence_after();
-              issue_kq(tmem + kColS, sK, next);  // S^T(u+1)
-              mma_commit(smem_u32(&bars->s_full));
-              ok = mbar_wait(smem_u32(&bars->dq_free), it & 1, abort, a.status);
-              if (!ok) break;
-              tc_fence_after();
-              issue_kq(tmem + kColDP, sV, next + Cfg::kTileBytes);  // dP^T(u+1)
-              mma_commit(smem_u32(&bars->dp_full));
-            }
-            continue;
-          }
           if (has_next) {
             ok = mbar_wait(smem_u32(&bars->st_full[sn]), ((st_it + 1) / Cfg::kStages) & 1, abort,
                            a.status);
@@ -869,9 +850,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float2 v = fmul2(pf, g);
             ds[c] = pack_bf16x2(v.x, v.y);
           }
-          // the causal dK (and without dQ, or at d = 64 non-causal, every dK)
-          // reads dS^T from TMEM
-          if constexpr (CAUSAL || !DQ || D == 64) tmem_st16(tDP + 16 * h, ds);
+          // the causal dK (and without dQ every dK) reads dS^T from TMEM
+          if constexpr (CAUSAL || !DQ) tmem_st16(tDP + 16 * h, ds);
           if constexpr (DQ) {
 #pragma unroll
             for (int u4 = 0; u4 < 4; ++u4) {
@@ -994,10 +974,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // lane = head-dim index dd, columns = the 128 queries of block i.
             // All 128 columns go to registers first and TMEM is released
             // before any atomic is issued, so the next dP^T never waits on them.
-            const int dd = wq * 32 + lane;
             int rows = min(kTile, nq_rows - i * kTile);
             if (!fa_dcheck(rows <= 0 || FA_IN_RANGE(i * kTile + rows - 1, nq_rows), a.status))
               rows = 0;  // debug build: the rows added lie inside the sequence's accumulator
+            if constexpr (Cfg::kDupK) {
+              // d = 64: warps 0 and 2 hold head dims 0-31, warps 1 and 3 dims
+              // 32-63 (rows 64-127 repeat rows 0-63); warps 0, 1 add query
+              // columns 0-63, warps 2, 3 columns 64-127
+              const int dd = (wq & 1) * 32 + lane;
+              const int qh = (wq >> 1) * 64;
+              float* dst = acc_base + (static_cast<size_t>(i) * kTile + qh) * D + dd;
+              uint32_t v[64];
+              tmem_ld64(t_lane + kColDP + qh, v);
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+#pragma unroll
+              for (int q = 0; q < 64; ++q)
+                if (qh + q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
+              continue;
+            }
+            const int dd = wq * 32 + lane;
             float* dst = acc_base + static_cast<size_t>(i) * kTile * D + dd;
             uint32_t v[64], w[64];
             tmem_ld64(t_lane + kColDP, v);

@@ -6,9 +6,10 @@
 //
 // Each pipe gets one kernel: 2 blocks of 1024 threads per SM (one full wave,
 // every warp slot used), each thread running 8 independent dependency chains
-// of the instruction for `iters` rounds between two clock64 reads. Thread 0
-// of every block records the block's cycle count; the largest over the grid
-// bounds the time the SM's 2 x 1024 x 8 x iters operations took.
+// of the instruction for `iters` rounds between two clock64 reads, each after
+// a block barrier. Thread 0 of every block records the block's cycle count;
+// the largest over the grid bounds the time the SM's 2 x 1024 x 8 x iters
+// operations took.
 
 #include <cstdint>
 
@@ -50,8 +51,10 @@ __global__ void __launch_bounds__(kRateThreads, 2)
       }
     }
   }
-  const unsigned long long t1 = clock64();
+  // every warp of the block has finished before the end time is read, so
+  // that thread 0's span covers the block's work
   __syncthreads();
+  const unsigned long long t1 = clock64();
   float acc = 0.f;
 #pragma unroll
   for (int c = 0; c < kRateChains; ++c) acc += x[c] + y[c];
