@@ -216,8 +216,23 @@ cudaError_t launch_varlen_check(const Problem& p, cudaStream_t stream) {
 }
 
 bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
-                   const Strides& s, int box_rows) {
+                   const Strides& s, int box_rows, int box_blocks) {
   if (!g_encode) return false;
+  if (box_blocks > 1) {
+    if (d % 64 != 0 || box_blocks > d / 64) return false;
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(d / 64),
+                                static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[4] = {static_cast<cuuint64_t>(s.row) * 2, 128,
+                                   static_cast<cuuint64_t>(s.head) * 2,
+                                   static_cast<cuuint64_t>(s.batch) * 2};
+    const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(box_rows),
+                               static_cast<cuuint32_t>(box_blocks), 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.row) * 2,

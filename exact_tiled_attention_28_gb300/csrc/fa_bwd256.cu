@@ -167,10 +167,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         {
           const uint32_t bar = smem_u32(&bars->kv_full);
           mbar_arrive_expect_tx(bar, 8 * kKBlk);
-          for (int cb = 0; cb < 4; ++cb) {
-            tma_load_4d(sK + cb * kKBlk, &tmK, bar, 64 * cb, j * kKeys, hh, bb, pol_kv);
-            tma_load_4d(sV + cb * kKBlk, &tmV, bar, 64 * cb, j * kKeys, hh, bb, pol_kv);
-          }
+          tma_load_5d(sK, &tmK, bar, 0, j * kKeys, 0, hh, bb, pol_kv);  // all four column blocks
+          tma_load_5d(sV, &tmV, bar, 0, j * kKeys, 0, hh, bb, pol_kv);
         }
         for (int i = i0; i < a.n_qb && ok; ++i, ++g) {
           const size_t row0 = static_cast<size_t>(bh) * a.Npad + static_cast<size_t>(i) * kTile;
@@ -179,8 +177,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
               return false;
             const uint32_t bar = smem_u32(&bars->q_full);
             mbar_arrive_expect_tx(bar, 4 * kQBlk + kTile * 4);
-            for (int cb = 0; cb < 4; ++cb)
-              tma_load_4d(sQ + cb * kQBlk, &tmQ, bar, 64 * cb, i * kTile, hh, bb, pol_qd);
+            tma_load_5d(sQ, &tmQ, bar, 0, i * kTile, 0, hh, bb, pol_qd);
             cp_bulk_g2s(s0 + kOffLse, a.lse2 + row0, kTile * 4, bar);
             return true;
           };
@@ -189,8 +186,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
               return false;
             const uint32_t bar = smem_u32(&bars->do_full);
             mbar_arrive_expect_tx(bar, 4 * kQBlk + kTile * 4);
-            for (int cb = 0; cb < 4; ++cb)
-              tma_load_4d(sDO + cb * kQBlk, &tmDO, bar, 64 * cb, i * kTile, hh, bb, pol_qd);
+            tma_load_5d(sDO, &tmDO, bar, 0, i * kTile, 0, hh, bb, pol_qd);
             cp_bulk_g2s(s0 + kOffDrow, a.Drow + row0, kTile * 4, bar);
             return true;
           };

@@ -155,8 +155,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         {
           const uint32_t bar = smem_u32(&bars->q_full);
           mbar_arrive_expect_tx(bar, kQBytes);
-          for (int cb = 0; cb < 4; ++cb)
-            tma_load_4d(sQ + cb * kBlk, &tmQ, bar, 64 * cb, qt * kTile, hh, bb, pol_q);
+          tma_load_5d(sQ, &tmQ, bar, 0, qt * kTile, 0, hh, bb, pol_q);  // all four column blocks
         }
         // tiles in the order the MMAs consume them: K(0), then K(j), V(j - 1)
         // for j = 1 .. J - 1, then V(J - 1) (see kv_load)
@@ -170,11 +169,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
             if (!ok) break;
             const uint32_t bar = smem_u32(&bars->kv_full[s]);
             const CUtensorMap* map = is_v ? &tmV : &tmK;
-            const int c0 = 128 * w;
-            mbar_arrive_expect_tx(bar, kHalfBytes);
-            tma_load_4d(sRing + s * kHalfBytes, map, bar, c0, tile * kTile, hh, bb, pol_kv);
-            tma_load_4d(sRing + s * kHalfBytes + kBlk, map, bar, c0 + 64, tile * kTile, hh, bb,
-                        pol_kv);
+            mbar_arrive_expect_tx(bar, kHalfBytes);  // column blocks 2w, 2w + 1 in one copy
+            tma_load_5d(sRing + s * kHalfBytes, map, bar, 0, tile * kTile, 2 * w, hh, bb, pol_kv);
           }
         }
       }
@@ -442,9 +438,10 @@ cudaError_t launch256_t(const Problem& p, const CUtensorMap& mq, const CUtensorM
 cudaError_t launch_fwd256(const Problem& p, const void* q, const void* k, const void* v, void* o,
                           float* lse, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
-  if (!make_tile_map(&mq, q, p.B, p.H, p.N, p.d, p.st[kQ]) ||
-      !make_tile_map(&mk, k, p.B, p.H, p.N, p.d, p.st[kK]) ||
-      !make_tile_map(&mv, v, p.B, p.H, p.N, p.d, p.st[kV]))
+  // 5-D maps: Q's copy spans all four 64-column blocks, a K or V half-tile's two
+  if (!make_tile_map(&mq, q, p.B, p.H, p.N, p.d, p.st[kQ], kTile, 4) ||
+      !make_tile_map(&mk, k, p.B, p.H, p.N, p.d, p.st[kK], kTile, 2) ||
+      !make_tile_map(&mv, v, p.B, p.H, p.N, p.d, p.st[kV], kTile, 2))
     return cudaErrorInvalidValue;
   Fwd256Args a;
   a.o = static_cast<__nv_bfloat16*>(o);

@@ -72,8 +72,12 @@ inline Strides contiguous_strides(int H, int N, int d) {
 // Encodes a 4-D TMA map (d, N, H, B) over a bf16 tensor with the given
 // strides, a {64, box_rows, 1, 1} box and 128-byte swizzle. Returns false on
 // failure.
+// box_blocks = 1: a 4-D map (d, row, head, batch) whose box is 64 columns by
+// box_rows rows. box_blocks > 1 (d a multiple of 64): a 5-D map (64 columns,
+// row, 64-column block, head, batch) whose box spans box_blocks blocks, for
+// tma_load_5d.
 bool make_tile_map(CUtensorMap* map, const void* base, int B, int H, int N, int d,
-                   const Strides& s, int box_rows = kTile);
+                   const Strides& s, int box_rows = kTile, int box_blocks = 1);
 
 // scale * log2(e), at least 1e-30, for the kernels that turn masked scores
 // into 2^-inf = 0 through their -inf value alone (the forwards), which needs
@@ -102,7 +106,8 @@ struct Bwd256Args {
   float scale, scale_log2;
   Strides sdk, sdv;
 };
-// maps: q and dO with 128-row boxes, k and v with 64-row boxes.
+// maps: 5-D (make_tile_map with box_blocks = 4), q and dO with 128-row
+// boxes, k and v with 64-row boxes; one copy fills a whole tile.
 cudaError_t launch_bwd256_dkdv(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mdo,
                                const Bwd256Args& a, cudaStream_t stream);

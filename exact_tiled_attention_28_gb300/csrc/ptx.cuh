@@ -207,6 +207,23 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 5-D tiled load (64 columns, row, 64-column block, head, batch): with a map
+// from make_tile_map(..., box_blocks > 1), one instruction fills box_blocks
+// 64-column blocks of a tile, in the layout that many 4-D loads would give
+// ([block][row][64 columns], 128-byte swizzle). A tensor copy occupies its
+// issuing thread for several hundred cycles whatever its size (measured on
+// GB300), so fewer, larger copies shorten a loader's critical path.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "l"(policy)
+      : "memory");
+}
+
 // Untiled bulk copy global -> shared of `bytes` (a multiple of 16, both
 // addresses 16-byte aligned), counted in bytes on the barrier.
 __device__ __forceinline__ void cp_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
