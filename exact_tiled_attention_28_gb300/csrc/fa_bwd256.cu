@@ -30,10 +30,16 @@
 // first, and dO_i follows after the dV MMAs; causal keeps dV first (measured
 // marginally faster). Both copies overlap the dQ^T MMAs.
 //
-// 384 threads: warp 0 TMA loader, warp 1 MMA issuer, warps 4-7 compute (one
-// thread per query row = TMEM lane), warps 8-11 dQ^T read-out and the dK /
-// dV epilogue (one thread per head-dim row of a half). Persistent, one CTA
-// per SM; every barrier wait is bounded.
+// 512 threads: warp 0 TMA loader, warp 1 MMA issuer, warps 4-7 compute (one
+// thread per query row = TMEM lane), warps 8-15 dQ^T read-out and the dK /
+// dV epilogue (one thread per head-dim row; warps 8-11 take query columns
+// 0-63 of each dQ^T half and head-dim half 0 of dK / dV, warps 12-15 the
+// rest). The read-out is the kernel's critical path: a dQ^T half's next
+// product waits for it, and each read-out warp's reductions issue one by
+// one, so eight warps halve it. Launched at 128 registers a thread, the
+// warpgroups rebalance with setmaxnreg: loader / MMA 96, compute 160,
+// read-out 128 (per SM sub-partition 96 + 160 + 128 + 128 = 512, the launch
+// total). Persistent, one CTA per SM; every barrier wait is bounded.
 
 #include <cuda_bf16.h>
 
@@ -45,7 +51,7 @@ namespace fa {
 namespace {
 
 constexpr int kKeys = 64;                 // keys per work item
-constexpr int kThreadsB = 384;
+constexpr int kThreadsB = 512;
 constexpr int kLoadWarpB = 0;
 constexpr int kMmaWarpB = 1;
 constexpr int kComputeWarp0 = 4;
@@ -124,9 +130,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     mbar_init(smem_u32(&bars->pds_ready), 4);  // one elected lane per compute warp
     mbar_init(smem_u32(&bars->pds_free), 1);
     mbar_init(smem_u32(&bars->dq_full), 1);
-    mbar_init(smem_u32(&bars->dq_free), 4);    // one elected lane per read-out warp
+    mbar_init(smem_u32(&bars->dq_free), 8);    // one elected lane per read-out warp
     mbar_init(smem_u32(&bars->acc_done), 1);
-    mbar_init(smem_u32(&bars->acc_free), 4);
+    mbar_init(smem_u32(&bars->acc_free), 8);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -146,6 +152,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  if (warp < kComputeWarp0) {
+    setmaxnreg_dec<96>();  // all of warps 0-3; 2 and 3 have no role
   if (warp == kLoadWarpB) {
     // ---------------------------------------------------------------- loader
     if (lane == 0) {
@@ -313,7 +321,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mma_commit(smem_u32(&bars->drain));
       mbar_drain(smem_u32(&bars->drain), 0, 1000000000ull);
     }
-  } else if (warp >= kComputeWarp0 && warp < kComputeWarp0 + 4) {
+  }
+  } else if (warp < kComputeWarp0 + 4) {
+    setmaxnreg_inc<160>();
     // ------------------------------------------------------ P and dS rows
     const int r = (warp - kComputeWarp0) * 32 + lane;  // query row = TMEM lane
     const uint32_t t_lane = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
@@ -389,9 +399,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         if (lane == 0) mbar_arrive(smem_u32(&bars->pds_ready));
       }
     }
-  } else if (warp >= kDqWarp0) {
+  } else {
     // ------------------------------------------ dQ^T read-out, dK / dV out
-    const int wq = warp & 3;
+    const int wq = warp & 3;             // TMEM lane quadrant: head dims 32 wq .. 32 wq + 31 of a half
+    const int rg = (warp - kDqWarp0) >> 2;  // query columns 64 rg .. 64 rg + 63; dK / dV half rg
     const uint32_t t_lane = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
     uint32_t it = 0, g = 0;
     bool ok = true;
@@ -411,26 +422,23 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           ok = mbar_wait_warp(smem_u32(&bars->dq_full), c & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
-          // lane = head dim dd, columns = the 128 queries of block i; TMEM is
-          // released before any reduction is issued
-          uint32_t v[64], w[64];
-          tmem_ld64(t_lane + kColDQ, v);
-          tmem_ld64(t_lane + kColDQ + 64, w);
+          // lane = head dim dd, columns = this warp's 64 queries of block i;
+          // TMEM is released before any reduction is issued
+          uint32_t v[64];
+          tmem_ld64(t_lane + kColDQ + 64 * rg, v);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
-          float* dst = acc_bh + static_cast<size_t>(i) * kTile * 256 + 128 * h + wq * 32 + lane;
+          float* dst = acc_bh + (static_cast<size_t>(i) * kTile + 64 * rg) * 256 + 128 * h +
+                       wq * 32 + lane;
 #pragma unroll
           for (int q = 0; q < 64; ++q)
-            if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * 256, __uint_as_float(v[q]));
-#pragma unroll
-          for (int q = 0; q < 64; ++q)
-            if (64 + q < rows)
-              atomicAdd(dst + static_cast<size_t>(64 + q) * 256, __uint_as_float(w[q]));
+            if (64 * rg + q < rows) atomicAdd(dst + static_cast<size_t>(q) * 256, __uint_as_float(v[q]));
         }
       }
       if (!ok) break;
-      // epilogue: dV = (dV^T)^T and dK = scale (dK^T)^T for the 64 keys
+      // epilogue: dV = (dV^T)^T and dK = scale (dK^T)^T for the 64 keys,
+      // head-dim half rg
       ok = mbar_wait_warp(smem_u32(&bars->acc_done), it & 1, abort, a.status);
       if (!ok) break;
       tc_fence_after();
@@ -446,20 +454,22 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                         static_cast<int64_t>(j * kKeys + keys - 1) * a.sdk.row, 256),
                      a.status))
         keys = 0;
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[64], w[64];
-        tmem_ld64(t_lane + kColDV + 64 * h, v);
-        tmem_ld64(t_lane + kColDK + 64 * h, w);
-        const int dd = 128 * h + wq * 32 + lane;
-        __nv_bfloat16* dvp = a.dv + bb * a.sdv.batch + hh * a.sdv.head +
-                             static_cast<int64_t>(j) * kKeys * a.sdv.row + dd;
-        __nv_bfloat16* dkp = a.dk + bb * a.sdk.batch + hh * a.sdk.head +
-                             static_cast<int64_t>(j) * kKeys * a.sdk.row + dd;
+      const int dd = 128 * rg + wq * 32 + lane;
+      __nv_bfloat16* dvp = a.dv + bb * a.sdv.batch + hh * a.sdv.head +
+                           static_cast<int64_t>(j) * kKeys * a.sdv.row + dd;
+      __nv_bfloat16* dkp = a.dk + bb * a.sdk.batch + hh * a.sdk.head +
+                           static_cast<int64_t>(j) * kKeys * a.sdk.row + dd;
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {  // 32 keys at a time
+        uint32_t v[32], w[32];
+        tmem_ld32(t_lane + kColDV + 64 * rg + 32 * cc, v);
+        tmem_ld32(t_lane + kColDK + 64 * rg + 32 * cc, w);
 #pragma unroll
-        for (int t = 0; t < 64; ++t) {
-          if (t < keys) {
-            dvp[t * a.sdv.row] = __float2bfloat16_rn(__uint_as_float(v[t]));
-            dkp[t * a.sdk.row] = __float2bfloat16_rn(__uint_as_float(w[t]) * a.scale);
+        for (int t = 0; t < 32; ++t) {
+          const int key = 32 * cc + t;
+          if (key < keys) {
+            dvp[key * a.sdv.row] = __float2bfloat16_rn(__uint_as_float(v[t]));
+            dkp[key * a.sdk.row] = __float2bfloat16_rn(__uint_as_float(w[t]) * a.scale);
           }
         }
       }
