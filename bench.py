@@ -87,7 +87,7 @@ def varlen_lengths(name):
 # (6 x 64 MiB) plus the fp32 dQ accumulator (128 MiB) = 537 MB at either size.
 NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.1925e8,
                            ("gpt_d64_n4096", False): 6.2250e8,
-                           ("dim_d256_n4096", False): 6.2123e8}
+                           ("dim_d256_n4096", False): 6.2199e8}
 
 
 def fwd_flops(B, H, N, d, causal):

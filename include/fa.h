@@ -263,8 +263,9 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
  * (the MUFU exponential), fma.rn.f32 and the two-lane fma.rn.f32x2 on every SM,
  * 2 blocks x 1024 threads x 8 chains x iters instructions per SM each.
  * cycles: DEVICE array of 6 unsigned 64-bit values, 8-byte aligned; after the
- * stream reaches the call, cycles[0], [2] and [4] hold the largest block's
- * clock64 cycle count of the ex2, FFMA and FFMA2 kernel (cycles[1], [3], [5]
+ * stream reaches the call, cycles[0], [2] and [4] hold the ex2, FFMA and
+ * FFMA2 kernel's longest SM span in clock64 cycles, from the earlier of the
+ * SM's two blocks' starts to the later of their ends (cycles[1], [3], [5]
  * are scratch). Operations per clock per SM = 16384 x iters / cycles (twice
  * that for FFMA2, which does two FMAs per instruction). iters in 1..2^20.
  */
