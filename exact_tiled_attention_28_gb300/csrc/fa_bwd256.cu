@@ -73,7 +73,7 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 256, kColDK = 
 
 struct BarsB256 {
   uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty;
-  uint64_t sdp_full, pds_ready, pds_free, dq_full, dq_free, acc_done, acc_free, drain;
+  uint64_t s_full, dp_full, pds_ready, pds_free, dq_full, dq_free, acc_done, acc_free, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     mbar_init(smem_u32(&bars->q_empty), 1);
     mbar_init(smem_u32(&bars->do_full), 1);
     mbar_init(smem_u32(&bars->do_empty), 1);
-    mbar_init(smem_u32(&bars->sdp_full), 1);
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->dp_full), 1);
     mbar_init(smem_u32(&bars->pds_ready), 4);  // one elected lane per compute warp
     mbar_init(smem_u32(&bars->pds_free), 1);
     mbar_init(smem_u32(&bars->dq_full), 1);
@@ -272,11 +273,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           if (!ok) break;
           tc_fence_after();
           issue_s(tmem + kColS, sQ, sK);
+          mma_commit(smem_u32(&bars->s_full));  // the compute warps start P while dP runs
           ok = mbar_wait(smem_u32(&bars->do_full), g & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
           issue_s(tmem + kColDP, sDO, sV);
-          mma_commit(smem_u32(&bars->sdp_full));
+          mma_commit(smem_u32(&bars->dp_full));
           // P and dS written, S and dP read out
           ok = mbar_wait(smem_u32(&bars->pds_ready), g & 1, abort, a.status);
           if (!ok) break;
@@ -337,26 +339,26 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       decode_b256(item, a, CAUSAL, bh, j);
       const int i0 = first_qblock(j, CAUSAL);
       for (int i = i0; i < a.n_qb; ++i, ++g) {
-        ok = mbar_wait_warp(smem_u32(&bars->sdp_full), g & 1, abort, a.status);
-        // the lse2 and D rows came with Q_i and dO_i
+        // phase A, P = exp2(S scale log2e - lse2), once S is in: it runs
+        // while the tensor core computes dP
+        ok = mbar_wait_warp(smem_u32(&bars->s_full), g & 1, abort, a.status);
+        // the lse2 rows came with Q_i
         if (ok) ok = mbar_wait_warp(smem_u32(&bars->q_full), g & 1, abort, a.status);
-        if (ok) ok = mbar_wait_warp(smem_u32(&bars->do_full), g & 1, abort, a.status);
         // the MMAs of the previous block have read P and dS
         if (ok && g > 0) ok = mbar_wait_warp(smem_u32(&bars->pds_free), (g - 1) & 1, abort, a.status);
         if (!ok) break;
         tc_fence_after();
-        const float l2 = sLse[r], dr = sDrow[r];
+        const float l2 = sLse[r];
         // last key column this row keeps: keys past N, and the causal diagonal
         int lim = min(kKeys - 1, a.N - 1 - j * kKeys);
         if (CAUSAL && i == i0) lim = min(lim, i * kTile + r - j * kKeys);
         const uint32_t prow = sP + r * 128, drow = sDS + r * 128;
-        // P and dS for 32 key columns; `mask` applies the causal diagonal and
-        // the keys past N. Two copies of the loop, so that blocks with nothing
-        // to mask (all but the diagonal and the last) run no select: selects
-        // in the loop cost 12% of the kernel.
+        // Two copies of the P loop, so that blocks with nothing to mask (all
+        // but the diagonal and the last) run no select: selects in the loop
+        // cost 12% of the kernel.
         const bool masked = lim < kKeys - 1;
-        auto p_ds = [&](int c, const uint32_t (&sv)[32], const uint32_t (&dv)[32], bool mask,
-                        uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+        float pf[64];  // P in fp32, for dS
+        auto p_row = [&](int c, const uint32_t (&sv)[32], bool mask, uint32_t (&pk)[16]) {
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
             const int k0 = 32 * c + 2 * t;
@@ -366,21 +368,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
               p0 = k0 > lim ? 0.f : p0;
               p1 = k0 + 1 > lim ? 0.f : p1;
             }
+            pf[k0] = p0;
+            pf[k0 + 1] = p1;
             pk[t] = pack_bf16x2(p0, p1);
-            dk[t] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * t]) - dr),
-                                p1 * (__uint_as_float(dv[2 * t + 1]) - dr));
           }
         };
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32], dv[32];
+          uint32_t sv[32];
           tmem_ld32(t_lane + kColS + 32 * c, sv);
-          tmem_ld32(t_lane + kColDP + 32 * c, dv);
-          uint32_t pk[16], dk[16];
+          uint32_t pk[16];
           if (masked)
-            p_ds(c, sv, dv, true, pk, dk);
+            p_row(c, sv, true, pk);
           else
-            p_ds(c, sv, dv, false, pk, dk);
+            p_row(c, sv, false, pk);
           // 16-byte chunk m of the row's 128 bytes sits at chunk m ^ (row & 7)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
@@ -388,6 +389,28 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + off),
                          "r"(pk[4 * m]), "r"(pk[4 * m + 1]), "r"(pk[4 * m + 2]), "r"(pk[4 * m + 3])
                          : "memory");
+          }
+        }
+        // phase B, dS = P (dP - D), once dP is in (the D rows came with dO_i)
+        ok = mbar_wait_warp(smem_u32(&bars->dp_full), g & 1, abort, a.status);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bars->do_full), g & 1, abort, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        const float dr = sDrow[r];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dv[32];
+          tmem_ld32(t_lane + kColDP + 32 * c, dv);
+          uint32_t dk[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int k0 = 32 * c + 2 * t;
+            dk[t] = pack_bf16x2(pf[k0] * (__uint_as_float(dv[2 * t]) - dr),
+                                pf[k0 + 1] * (__uint_as_float(dv[2 * t + 1]) - dr));
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t off = static_cast<uint32_t>(((4 * c + m) ^ (r & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(drow + off),
                          "r"(dk[4 * m]), "r"(dk[4 * m + 1]), "r"(dk[4 * m + 2]), "r"(dk[4 * m + 3])
                          : "memory");
