@@ -1253,10 +1253,12 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* k, const voi
   const int BH = p.B * p.H;
   CUtensorMap maps[4];
   const int kv_rows = p.d == 256 ? 64 : kTile;  // the d = 256 kernel takes 64-key blocks
-  const int blocks = p.d == 256 ? 4 : 1;         // and loads whole rows with 5-D copies
+  // and loads whole tiles with 5-D copies (q causal: in two halves)
+  const int blocks = p.d == 256 ? 4 : 1;
   if (p.dq_separate && !bwd_dq_separate_supported(p.d)) return cudaErrorInvalidValue;
   if ((stages & (p.dq_separate ? (kStageDkdv | kStageDq) : kStageDkdv)) &&
-      (!make_tile_map(&maps[0], q, p.B, p.H, p.N, p.d, p.st[kQ], kTile, blocks) ||
+      (!make_tile_map(&maps[0], q, p.B, p.H, p.N, p.d, p.st[kQ], kTile,
+                      p.d == 256 && p.causal ? 2 : blocks) ||
        !make_tile_map(&maps[1], k, p.B, p.H, p.N, p.d, p.st[kK], kv_rows, blocks) ||
        !make_tile_map(&maps[2], v, p.B, p.H, p.N, p.d, p.st[kV], kv_rows, blocks) ||
        !make_tile_map(&maps[3], dO, p.B, p.H, p.N, p.d, p.st[kdO], kTile, blocks)))

@@ -72,7 +72,8 @@ constexpr uint32_t kTmemColsB = 512;
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 256, kColDK = 384;
 
 struct BarsB256 {
-  uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty;
+  uint64_t kv_full, kv_empty, do_full, do_empty;
+  uint64_t q_full[2], q_empty[2];  // Q_i (causal: in two 128-column halves)
   uint64_t s_full, dp_full, pds_ready, pds_free, dq_full, dq_free, acc_done, acc_free, drain;
   uint32_t tmem_base;
   int abort;
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  constexpr int kQParts = CAUSAL ? 2 : 1;  // copies (and barriers) per Q_i
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sQ = s0 + kOffQ, sDO = s0 + kOffDO, sK = s0 + kOffK, sV = s0 + kOffV;
   const uint32_t sP = s0 + kOffP, sDS = s0 + kOffDS;
@@ -122,8 +124,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->kv_full), 1);
     mbar_init(smem_u32(&bars->kv_empty), 1);
-    mbar_init(smem_u32(&bars->q_full), 1);
-    mbar_init(smem_u32(&bars->q_empty), 1);
+    for (int hq = 0; hq < 2; ++hq) {
+      mbar_init(smem_u32(&bars->q_full[hq]), 1);
+      mbar_init(smem_u32(&bars->q_empty[hq]), 1);
+    }
     mbar_init(smem_u32(&bars->do_full), 1);
     mbar_init(smem_u32(&bars->do_empty), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
@@ -181,13 +185,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         for (int i = i0; i < a.n_qb && ok; ++i, ++g) {
           const size_t row0 = static_cast<size_t>(bh) * a.Npad + static_cast<size_t>(i) * kTile;
+          // Causal, Q_i comes in two halves of two column blocks: the dK^T
+          // half that reads each releases it, and S's first eight K steps
+          // need only the first (measured 3.8% faster causal, 2.6% slower
+          // non-causal, which loads Q_i with one copy)
           auto load_q = [&]() {
-            if (g > 0 && !mbar_wait(smem_u32(&bars->q_empty), (g - 1) & 1, abort, a.status))
-              return false;
-            const uint32_t bar = smem_u32(&bars->q_full);
-            mbar_arrive_expect_tx(bar, 4 * kQBlk + kTile * 4);
-            tma_load_5d(sQ, &tmQ, bar, 0, i * kTile, 0, hh, bb, pol_qd);
-            cp_bulk_g2s(s0 + kOffLse, a.lse2 + row0, kTile * 4, bar);
+            for (int hq = 0; hq < kQParts; ++hq) {
+              if (g > 0 &&
+                  !mbar_wait(smem_u32(&bars->q_empty[hq]), (g - 1) & 1, abort, a.status))
+                return false;
+              const uint32_t bar = smem_u32(&bars->q_full[hq]);
+              mbar_arrive_expect_tx(bar, 4 * kQBlk / kQParts + (hq == 0 ? kTile * 4 : 0));
+              tma_load_5d(sQ + 2 * hq * kQBlk, &tmQ, bar, 0, i * kTile, 2 * hq, hh, bb, pol_qd);
+              if (hq == 0) cp_bulk_g2s(s0 + kOffLse, a.lse2 + row0, kTile * 4, bar);
+            }
             return true;
           };
           auto load_do = [&]() {
@@ -215,8 +226,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const uint32_t ph = (g - 1) & 1;
         if (ok) ok = mbar_wait(smem_u32(&bars->do_empty), ph, abort, a.status);
         if (!ok) mbar_drain(smem_u32(&bars->do_full), ph, 100000000ull);
-        if (ok) ok = mbar_wait(smem_u32(&bars->q_empty), ph, abort, a.status);
-        if (!ok) mbar_drain(smem_u32(&bars->q_full), ph, 100000000ull);
+        for (int hq = 0; hq < kQParts; ++hq) {
+          if (ok) ok = mbar_wait(smem_u32(&bars->q_empty[hq]), ph, abort, a.status);
+          if (!ok) mbar_drain(smem_u32(&bars->q_full[hq]), ph, 100000000ull);
+        }
       }
     }
   } else if (warp == kMmaWarpB) {
@@ -230,6 +243,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       auto issue_s = [&](uint32_t dst, uint32_t x, uint32_t y) {
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
+          const uint32_t ox = (kk >> 2) * kQBlk + (kk & 3) * 32;
+          const uint32_t oy = (kk >> 2) * kKBlk + (kk & 3) * 32;
+          mma_ss(dst, desc_at(make_desc_sw128(opaque_u32(x + ox), 16, 1024), 0),
+                 desc_at(make_desc_sw128(opaque_u32(y + oy), 16, 1024), 0), idesc_s, kk > 0);
+        }
+      };
+      // the same over head dims 128 h .. 128 h + 127 (K steps 8 h .. 8 h + 7)
+      auto issue_s_half = [&](uint32_t dst, uint32_t x, uint32_t y, int h) {
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8) {
+          const int kk = 8 * h + k8;
           const uint32_t ox = (kk >> 2) * kQBlk + (kk & 3) * 32;
           const uint32_t oy = (kk >> 2) * kKBlk + (kk & 3) * 32;
           mma_ss(dst, desc_at(make_desc_sw128(opaque_u32(x + ox), 16, 1024), 0),
@@ -269,10 +293,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tc_fence_after();
         for (int i = i0; i < a.n_qb && ok; ++i, ++g) {
           const bool first = i == i0;
-          ok = mbar_wait(smem_u32(&bars->q_full), g & 1, abort, a.status);
+          ok = mbar_wait(smem_u32(&bars->q_full[0]), g & 1, abort, a.status);
           if (!ok) break;
           tc_fence_after();
-          issue_s(tmem + kColS, sQ, sK);
+          if constexpr (kQParts == 2) {
+            issue_s_half(tmem + kColS, sQ, sK, 0);  // head dims 0-127: Q_i's first half
+            ok = mbar_wait(smem_u32(&bars->q_full[1]), g & 1, abort, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s_half(tmem + kColS, sQ, sK, 1);
+          } else {
+            issue_s(tmem + kColS, sQ, sK);
+          }
           mma_commit(smem_u32(&bars->s_full));  // the compute warps start P while dP runs
           ok = mbar_wait(smem_u32(&bars->do_full), g & 1, abort, a.status);
           if (!ok) break;
@@ -293,15 +325,16 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           if constexpr (!CAUSAL) {
             issue_g(tmem + kColDK, sQ, 0, sDS, !first);
             issue_g(tmem + kColDK + 64, sQ, 1, sDS, !first);
-            mma_commit(smem_u32(&bars->q_empty));
+            mma_commit(smem_u32(&bars->q_empty[0]));
           }
           issue_g(tmem + kColDV, sDO, 0, sP, !first);
           issue_g(tmem + kColDV + 64, sDO, 1, sP, !first);
           mma_commit(smem_u32(&bars->do_empty));
           if constexpr (CAUSAL) {
             issue_g(tmem + kColDK, sQ, 0, sDS, !first);
+            mma_commit(smem_u32(&bars->q_empty[0]));
             issue_g(tmem + kColDK + 64, sQ, 1, sDS, !first);
-            mma_commit(smem_u32(&bars->q_empty));
+            mma_commit(smem_u32(&bars->q_empty[1]));
           }
           for (int h = 0; h < 2 && ok; ++h) {
             const uint32_t c = 2 * g + h;  // dQ^T halves issued so far
@@ -343,7 +376,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         // while the tensor core computes dP
         ok = mbar_wait_warp(smem_u32(&bars->s_full), g & 1, abort, a.status);
         // the lse2 rows came with Q_i
-        if (ok) ok = mbar_wait_warp(smem_u32(&bars->q_full), g & 1, abort, a.status);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bars->q_full[0]), g & 1, abort, a.status);
         // the MMAs of the previous block have read P and dS
         if (ok && g > 0) ok = mbar_wait_warp(smem_u32(&bars->pds_free), (g - 1) & 1, abort, a.status);
         if (!ok) break;

@@ -106,8 +106,9 @@ struct Bwd256Args {
   float scale, scale_log2;
   Strides sdk, sdv;
 };
-// maps: 5-D (make_tile_map with box_blocks = 4), q and dO with 128-row
-// boxes, k and v with 64-row boxes; one copy fills a whole tile.
+// maps: 5-D (make_tile_map with box_blocks = 4; q causal with 2), q and dO
+// with 128-row boxes, k and v with 64-row boxes; a copy fills a whole tile
+// (q causal: half a tile).
 cudaError_t launch_bwd256_dkdv(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mdo,
                                const Bwd256Args& a, cudaStream_t stream);
