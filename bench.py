@@ -537,6 +537,11 @@ def run_varlen(args):
         "gpu_launches": 6 * args.steps,
         "clocks": clocks,
     }
+    g_ms = replicas.max_over_ranks(graph_step_ms(fa, torch, step, args.steps), dev)
+    line["graph"] = {"ms_per_step": g_ms,
+                     "fwd_bwd_tflops": replicas.aggregate_throughput(3.5 * F, world, g_ms),
+                     "how": "one step captured into a CUDA graph, replayed `steps` times "
+                            "after the timed region; same kernels, no per-call host work"}
     if world > 1:
         torch.distributed.barrier()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -820,6 +825,8 @@ def sub_line(fa, torch, inputs, dev, stream, seed, name, causal, steps, warmup, 
     fwd_tf = F / (t["fwd_ms"] * 1e-3) / 1e12
     dkdv_tf = 2.5 * F / (t["dkdv_ms"] * 1e-3) / 1e12
     fb_tf = 3.5 * F / ((t["fwd_ms"] + t["bwd_ms"]) * 1e-3) / 1e12
+    g_ms = graph_step_ms(fa, torch, lambda: pb.step(fa, torch.cuda.current_stream(), causal,
+                                                    scale), steps)
     kd, kf = kernel_names(d)
     del pb
     torch.cuda.empty_cache()
@@ -828,9 +835,42 @@ def sub_line(fa, torch, inputs, dev, stream, seed, name, causal, steps, warmup, 
             "steps": steps, **{k: v for k, v in t.items()},
             "fwd_tflops": fwd_tf, "fwd_frac_of_burst_peak": fwd_tf / peaks["burst"],
             "fwd_bwd_tflops": fb_tf, "fwd_bwd_frac_of_burst_peak": fb_tf / peaks["burst"],
+            "graph": {"ms_per_step": g_ms, "fwd_bwd_tflops": 3.5 * F / (g_ms * 1e-3) / 1e12},
             "roofline": tensor_roofline(kd, dkdv_tf, peaks, f"2.5 x 4*B*H*N^2*d"
                                         f"{' / 2' if causal else ''} = {2.5 * F:.4g} FLOP per launch"),
             "roofline_fwd": tensor_roofline(kf, fwd_tf, peaks, f"{F:.4g} FLOP per launch")}
+
+
+def graph_step_ms(fa, torch, run, steps):
+    """One step (run() enqueues fa_fwd + fa_bwd on the current stream)
+    captured into a CUDA graph, then replayed `steps` times back to back: the
+    step time without the host's per-call work (argument checks, tensor maps,
+    launches). Small workloads are bound by that work when launched call by
+    call."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status reports an error in the graph replays")
+    del g
+    return t0.elapsed_time(t1) / steps
 
 
 def sustained_leg(fa, torch, pb, stream, causal, scale, seconds, uuid, peaks):
@@ -955,6 +995,14 @@ def run_ours(args):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    if args.layout == "bhnd":
+        g_ms = replicas.max_over_ranks(
+            graph_step_ms(fa, torch, lambda: pb.step(fa, torch.cuda.current_stream(), causal,
+                                                     scale), args.steps), dev)
+        line["graph"] = {"ms_per_step": g_ms,
+                         "fwd_bwd_tflops": replicas.aggregate_throughput(3.5 * F, world, g_ms),
+                         "how": "one step captured into a CUDA graph, replayed `steps` times "
+                                "after the timed region; same kernels, no per-call host work"}
     if not args.no_extra_legs and args.layout == "bhnd":
         line["sustained"] = sustained_leg(fa, torch, pb, stream, causal, scale,
                                           SUSTAINED_LEG_S, uuid, peaks)

@@ -34,6 +34,12 @@
  *  - stream is a cudaStream_t (NULL = the legacy default stream). Every call
  *    only enqueues work and returns; outputs are valid once the stream has
  *    reached that point. No call synchronises the device.
+ *  - So the attention calls (forward, backward and its stages, the packed-
+ *    batch pair, decode) can be captured into a CUDA graph on a capturing
+ *    stream. Each replay runs the same kernels on the buffers as they are
+ *    at replay time; pointers, sizes and scale are fixed at capture. Make
+ *    one ordinary call on the device before capturing, so that the
+ *    per-device set-up below is not done inside the capture.
  *  - Argument errors are reported before anything is enqueued, and the
  *    outputs are then untouched. Launch failures return FA_ERR_CUDA.
  *  - A kernel that waits on an on-chip barrier for longer than 2 s gives up,
