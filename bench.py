@@ -85,8 +85,8 @@ def varlen_lengths(name):
 # workload and causal flag; None where no capture of the current kernel exists.
 # Algorithmic bytes for comparison: q, k, v, dO read and dk, dv written once
 # (6 x 64 MiB) plus the fp32 dQ accumulator (128 MiB) = 537 MB at either size.
-NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.1882e8,
-                           ("gpt_d64_n4096", False): 6.2250e8,
+NCU_TRAFFIC_BYTES: dict = {("gpt_d128_n4096", False): 6.1875e8,
+                           ("gpt_d64_n4096", False): 6.2160e8,
                            ("dim_d256_n4096", False): 6.2114e8}
 
 
